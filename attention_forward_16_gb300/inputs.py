@@ -1,0 +1,83 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module holds no attention arithmetic: it only draws Q, K, V.  Both the
+CUDA path (tests, ``bench.py``) and the float64 oracle consume what it makes.
+
+Recipe: a NumPy ``Generator(PCG64(seed))`` draws Q, then K, then V, each as
+float32 standard normal of shape [B, H, N, D]; each is multiplied by
+``input_scale`` (a power of two, so exact) and then rounded to the working
+dtype (fp16 / bf16 via torch's round-to-nearest-even cast, fp32 unchanged).
+The oracle upcasts the rounded values to float64, so both sides see exactly
+the same numbers.
+
+The workloads mirror the pages' benchmark shapes: "FlashAttention under the
+catlass template", section "Performance data" (B=4, H=32, N=4096, D=128 fp16
+``torch.randn`` inputs), plus the small, causal, bf16 and sliding-window cases
+listed in :data:`WORKLOADS`.
+"""
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_WINDOW = 2
+
+_TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str          # "f16" | "bf16" | "f32"
+    scale: float
+    mask: int
+    win_l: int = -1
+    win_r: int = -1
+    input_scale: float = 1.0
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+
+WORKLOADS = {
+    "tiny_f32_full": Workload("tiny_f32_full", 1, 2, 128, 64, "f32", 1.0 / 8.0, MASK_NONE, seed=1001),
+    "tiny_f32_causal": Workload("tiny_f32_causal", 1, 2, 128, 64, "f32", 1.0 / 8.0, MASK_CAUSAL, seed=1001),
+    "f16_causal_1k": Workload("f16_causal_1k", 2, 8, 1024, 64, "f16", 0.125, MASK_CAUSAL, seed=1002),
+    "f16_full_4k": Workload("f16_full_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128), MASK_NONE, seed=1003),
+    "f16_causal_4k": Workload("f16_causal_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128), MASK_CAUSAL, seed=1004),
+    "bf16_causal_4k": Workload("bf16_causal_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128), MASK_CAUSAL, seed=1004),
+    "bf16_full_4k": Workload("bf16_full_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128), MASK_NONE, seed=1003),
+    "bf16_window_16k": Workload("bf16_window_16k", 1, 64, 16384, 128, "bf16", 1.0 / math.sqrt(128),
+                                MASK_WINDOW, 1024, 0, input_scale=0.5, seed=1005),
+}
+
+
+def torch_dtype(name):
+    return _TORCH_DTYPES[name]
+
+
+def make_qkv(B, H, N, D, dtype="f16", seed=0, input_scale=1.0, n_k=None):
+    """Draw Q [B,H,N,D] and K, V [B,H,n_k,D] (n_k defaults to N) on the CPU.
+
+    Returns three contiguous CPU torch tensors of the working dtype.
+    """
+    n_k = N if n_k is None else n_k
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for shape in ((B, H, N, D), (B, H, n_k, D), (B, H, n_k, D)):
+        x = rng.standard_normal(size=shape, dtype=np.float32)
+        if input_scale != 1.0:
+            x *= np.float32(input_scale)
+        out.append(torch.from_numpy(x).to(_TORCH_DTYPES[dtype]).contiguous())
+    return tuple(out)
+
+
+def make_workload(w: Workload):
+    return make_qkv(w.B, w.H, w.N, w.D, w.dtype, w.seed, w.input_scale)
