@@ -1,0 +1,191 @@
+"""ctypes binding over libfa.so: argument marshalling only.
+
+The functions named like the C ABI (``fa_fwd``, ``fa_fwd_f16`` ...) take raw
+pointers and sizes exactly as ``include/fa.h`` declares them.
+:func:`attention_fwd` is the tensor-level convenience: it checks shapes,
+allocates O and LSE with torch on the inputs' device and calls ``fa_fwd_ex``
+on the current stream.  Every step of the computation runs in libfa's CUDA
+kernels; there is no other implementation to fall back to, and a missing
+library raises.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_WINDOW = 0, 1, 2
+FA_F16, FA_BF16, FA_F32 = 0, 1, 2
+FA_OK, FA_ERR_ARG, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+
+_DTYPE_CODE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32}
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+# name -> (restype, argtypes), mirroring include/fa.h
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _I, _P]),
+    "fa_fwd_f16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_bf16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
+    "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
+    "fa_device_status": (_I, [_P]),
+    "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
+    "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
+    "fa_plan_units": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), _I]),
+    "fa_tile_needs_mask": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_last_cuda_error": (ctypes.c_char_p, []),
+    "fa_version": (_I, []),
+}
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code, where):
+        lib = load()
+        msg = lib.fa_strerror(code).decode()
+        if code == FA_ERR_CUDA:
+            msg += ": " + lib.fa_last_cuda_error().decode()
+        super().__init__(f"{where} returned {code} ({msg})")
+        self.code = code
+
+
+def load(path=None):
+    """Load libfa.so (built by ``attention_forward_16_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libfa.so is not built ({p}); run attention_forward_16_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc, where):
+    if rc != FA_OK:
+        raise FaError(rc, where)
+    return rc
+
+
+# ---------------------------------------------------------------- raw C ABI
+
+def fa_fwd(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, stream):
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, stream)
+
+
+def fa_fwd_f16(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream):
+    return load().fa_fwd_f16(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream)
+
+
+def fa_fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream):
+    return load().fa_fwd_bf16(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream)
+
+
+def fa_fwd_f32(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream):
+    return load().fa_fwd_f32(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stream)
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, stream):
+    return load().fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, stream)
+
+
+def fa_device_status(stream=None):
+    return load().fa_device_status(stream)
+
+
+def fa_set_wait_limit_ns(ns):
+    return load().fa_set_wait_limit_ns(ns)
+
+
+def fa_selftest_wait_timeout(limit_ns, stream=None):
+    return load().fa_selftest_wait_timeout(limit_ns, stream)
+
+
+def fa_plan_units(B, H, N, mask_kind, win_l=-1, win_r=-1):
+    """All work units as a list of (bh, q0, lo0, hi0, lo1, hi1)."""
+    lib = load()
+    n = lib.fa_plan_units(B, H, N, mask_kind, win_l, win_r, None, 0)
+    _check(n if n < 0 else 0, "fa_plan_units")
+    buf = (ctypes.c_int * (6 * n))()
+    lib.fa_plan_units(B, H, N, mask_kind, win_l, win_r, buf, n)
+    return [tuple(buf[6 * u:6 * u + 6]) for u in range(n)]
+
+
+def fa_tile_needs_mask(N, mask_kind, win_l, win_r, r0, j):
+    return load().fa_tile_needs_mask(N, mask_kind, win_l, win_r, r0, j)
+
+
+# ------------------------------------------------------------ tensor level
+
+def mask_args(causal=False, window=None):
+    """(mask_kind, win_l, win_r) from the user-level mask options."""
+    if window is not None:
+        if causal:
+            raise ValueError("give either causal=True or window=(left, right), not both")
+        wl, wr = window
+        return FA_MASK_WINDOW, -1 if wl is None else int(wl), -1 if wr is None else int(wr)
+    return (FA_MASK_CAUSAL, -1, -1) if causal else (FA_MASK_NONE, -1, -1)
+
+
+def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, out=None, lse=None,
+                  stream=None):
+    """O, LSE = softmax(scale * Q K^T + mask) V for [B, H, N, D] CUDA tensors.
+
+    ``window=(left, right)`` selects the sliding window (None or -1 for an
+    unbounded side); ``scale`` defaults to 1/sqrt(D); ``o_dtype=torch.float32``
+    returns O in fp32 for 16-bit inputs.  Runs on the current CUDA stream
+    unless ``stream`` (a torch.cuda.Stream) is given.
+    """
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError(f"q, k, v must share one [B, H, N, D] shape, got {tuple(q.shape)}, "
+                         f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
+        raise ValueError("q, k, v must share one dtype among float16, bfloat16, float32")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mk, wl, wr = mask_args(causal, window)
+    od = q.dtype if o_dtype is None else o_dtype
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=od, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od], s)
+    _check(rc, "fa_fwd_ex")
+    return out, lse
+
+
+def attention_fwd_host(q, k, v, device="cuda", **kw):
+    """The same call for host tensors: copies Q, K, V to the device, runs the
+    fused forward, and copies O and LSE back (pinned host buffers make both
+    copies asynchronous)."""
+    dq, dk, dv = (t.to(device, non_blocking=True) for t in (q, k, v))
+    o, lse = attention_fwd(dq, dk, dv, **kw)
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    ho.copy_(o, non_blocking=True)
+    hl.copy_(lse, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return ho, hl

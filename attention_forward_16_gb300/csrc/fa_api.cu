@@ -1,0 +1,301 @@
+// C ABI of libfa: argument validation, mask normalisation, TMA descriptor
+// encoding, kernel dispatch, device status word.
+//
+// The two-phase "workspace size + execute" call of the ops-transformer
+// walk-through (section "the complete operator in ops-transformer", aclnn
+// FlashAttention call) is not needed here: the kernels use no workspace, so
+// one call enqueues the whole forward on the caller's stream.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_cuda_err[256] = "no error";
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+__device__ int g_status_word;
+
+struct DeviceInfo {
+    std::once_flag once;
+    int sms = 0;
+    int* status = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+cudaError_t g_encode_err = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_cuda_err, sizeof(g_last_cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+}
+
+int cuda_fail_msg(const char* msg) {
+    std::snprintf(g_last_cuda_err, sizeof(g_last_cuda_err), "%s", msg);
+    return FA_ERR_CUDA;
+}
+
+// Per-device facts, resolved once with that device current.
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail_msg("device ordinal out of range");
+    DeviceInfo& d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+    });
+    if (d.err != cudaSuccess) return cuda_fail(d.err);
+    *out = &d;
+    return FA_OK;
+}
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess) g_encode_err = cudaErrorSymbolNotFound;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (g_encode_err != cudaSuccess || !g_encode) return cuda_fail(g_encode_err);
+    *fn = g_encode;
+    return FA_OK;
+}
+
+// 3-D view [B*H][N][D] of a 16-bit tensor; box = 128 rows x 64 columns
+// (128 bytes: the widest box the 128-byte swizzle allows).
+int make_map(CUtensorMap* m, const void* base, bool bf16, int BH, int N, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    int rc = encoder(&enc);
+    if (rc != FA_OK) return rc;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)fa::kTileM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_last_cuda_err, sizeof(g_last_cuda_err), "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Normalised mask: causal == window(-1, 0), none == window(-1, -1).
+int normalise_mask(int mask_kind, int win_l, int win_r, int N, fa::Geom* g) {
+    g->N = N;
+    switch (mask_kind) {
+        case FA_MASK_NONE: g->win_l = -1; g->win_r = -1; return FA_OK;
+        case FA_MASK_CAUSAL: g->win_l = -1; g->win_r = 0; return FA_OK;
+        case FA_MASK_WINDOW:
+            if (win_l < -1 || win_r < -1) return FA_ERR_ARG;
+            g->win_l = win_l;
+            g->win_r = win_r;
+            return FA_OK;
+        default: return FA_ERR_ARG;
+    }
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
+             int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, fa::Geom* g) {
+    if (!q || !k || !v || !o) return FA_ERR_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || D <= 0) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    int rc = normalise_mask(mask_kind, win_l, win_r, N, g);
+    if (rc != FA_OK) return rc;
+    const long long bh = (long long)B * H;
+    if (bh > 0x7fffffffLL) return FA_ERR_ARG;
+    const double elems = (double)bh * N * D;
+    if (elems > 4.0e18) return FA_ERR_ARG;
+    switch (dtype) {
+        case FA_F16:
+        case FA_BF16:
+            if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+            if (o_dtype != dtype && o_dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+            break;
+        case FA_F32:
+            if (D > 128) return FA_ERR_UNSUPPORTED;
+            if (o_dtype != FA_F32) return FA_ERR_UNSUPPORTED;
+            break;
+        default: return FA_ERR_UNSUPPORTED;
+    }
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
+    if (lse && !aligned(lse, 4)) return FA_ERR_ALIGN;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+              float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, void* stream) {
+    fa::Geom g;
+    int rc = validate(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, &g);
+    if (rc != FA_OK) return rc;
+    DeviceInfo* dev;
+    if ((rc = device_info(&dev)) != FA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+
+    if (dtype == FA_F32) {
+        fa::SimtParams p;
+        p.q = static_cast<const float*>(q);
+        p.k = static_cast<const float*>(k);
+        p.v = static_cast<const float*>(v);
+        p.o = static_cast<float*>(o);
+        p.lse = lse;
+        p.g = g;
+        p.BH = BH;
+        p.D = D;
+        p.scale = scale;
+        cudaError_t e = fa::launch_simt_f32(p, s);
+        return e == cudaSuccess ? FA_OK : cuda_fail(e);
+    }
+
+    const bool bf16 = dtype == FA_BF16;
+    fa::TcParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = make_map(&p.tm_q, q, bf16, BH, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_k, k, bf16, BH, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_v, v, bf16, BH, N, D)) != FA_OK) return rc;
+    p.o = o;
+    p.lse = lse;
+    p.g = g;
+    p.BH = BH;
+    const long long units = (long long)BH * fa::n_pairs_for(N);
+    if (units > 0x7fffffffLL) return FA_ERR_ARG;
+    p.n_units = (int)units;
+    p.order = fa::unit_order_for(g);
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.o_f32 = o_dtype == FA_F32 ? 1 : 0;
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.status = dev->status;
+    const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
+    cudaError_t e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D, float scale,
+           int mask_kind, int win_l, int win_r, int dtype, void* stream) {
+    return fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, dtype, stream);
+}
+
+int fa_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+               float scale, int mask_kind, int win_l, int win_r, void* stream) {
+    return fa_fwd(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, FA_F16, stream);
+}
+
+int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                float scale, int mask_kind, int win_l, int win_r, void* stream) {
+    return fa_fwd(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, FA_BF16, stream);
+}
+
+int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+               float scale, int mask_kind, int win_l, int win_r, void* stream) {
+    return fa_fwd(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, FA_F32, stream);
+}
+
+int fa_device_status(void* stream) {
+    DeviceInfo* dev;
+    int rc = device_info(&dev);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cuda_fail(e);
+        return FA_ERR_DEVICE;
+    }
+    int word = 0;
+    e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        cuda_fail(e);
+        return FA_ERR_DEVICE;
+    }
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            cuda_fail(e);
+            return FA_ERR_DEVICE;
+        }
+        return FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+unsigned long long fa_set_wait_limit_ns(unsigned long long ns) {
+    if (ns == 0) ns = 1;
+    return g_wait_limit_ns.exchange(ns);
+}
+
+int fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+    DeviceInfo* dev;
+    int rc = device_info(&dev);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = fa::launch_selftest_timeout(dev->status, limit_ns, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int* out, int cap) {
+    if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_ARG;
+    fa::Geom g;
+    int rc = normalise_mask(mask_kind, win_l, win_r, N, &g);
+    if (rc != FA_OK) return rc;
+    const long long units = (long long)B * H * fa::n_pairs_for(N);
+    if (units > 0x7fffffffLL) return FA_ERR_ARG;
+    const int order = fa::unit_order_for(g);
+    for (int u = 0; out && u < cap && u < units; ++u) {
+        fa::Unit un = fa::make_unit(g, B * H, order, u);
+        int* r = out + 6 * u;
+        r[0] = un.bh;
+        r[1] = un.q0;
+        r[2] = un.lo[0];
+        r[3] = un.hi[0];
+        r[4] = un.lo[1];
+        r[5] = un.hi[1];
+    }
+    return (int)units;
+}
+
+int fa_tile_needs_mask(int N, int mask_kind, int win_l, int win_r, int r0, int j) {
+    fa::Geom g;
+    if (normalise_mask(mask_kind, win_l, win_r, N, &g) != FA_OK) return FA_ERR_ARG;
+    return fa::tile_needs_mask(g, r0, j) ? 1 : 0;
+}
+
+const char* fa_strerror(int code) {
+    switch (code) {
+        case FA_OK: return "ok";
+        case FA_ERR_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported dtype or head dimension";
+        case FA_ERR_ALIGN: return "pointer not aligned (16 bytes for q/k/v/o, 4 for lse)";
+        case FA_ERR_CUDA: return "CUDA error (see fa_last_cuda_error)";
+        case FA_ERR_TIMEOUT: return "a kernel wait timed out";
+        case FA_ERR_DEVICE: return "device error reported by the stream";
+        default: return "unknown error code";
+    }
+}
+
+const char* fa_last_cuda_error(void) { return g_last_cuda_err; }
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

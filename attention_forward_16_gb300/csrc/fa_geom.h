@@ -1,0 +1,148 @@
+// Tile geometry shared by the host planner and the kernels: which key tiles a
+// block of query rows must visit under a mask, which of those need
+// per-element masking, and how persistent CTAs enumerate work units.
+//
+// Mask semantics ("Ascend C advanced practice: high-performance
+// FlashAttention-2-style tile-level fused attention", section 4.2 for causal;
+// "FlashAttention under the catlass template", section "Usage" for the
+// (window_left, window_right) tuple): key j is visible to query i iff
+//     (win_l < 0 || j >= i - win_l) && (win_r < 0 || j <= i + win_r) && j < N.
+// Causal is the window (-1, 0) and no mask is (-1, -1).  Skipping key tiles
+// that are wholly masked is the causal block skip of that page's section 6,
+// generalised to the window.
+#pragma once
+
+#ifdef __CUDACC__
+#define FA_HD __host__ __device__ __forceinline__
+#else
+#define FA_HD inline
+#endif
+
+namespace fa {
+
+constexpr int kTileM = 128;  // query rows per Q tile (one tcgen05 M=128 accumulator)
+constexpr int kTileN = 128;  // keys per K/V tile
+
+// Unit enumeration orders (longest-first for masks whose work grows with q).
+enum UnitOrder { ORDER_HEAD_MAJOR = 0, ORDER_Q_DESC = 1, ORDER_Q_ASC = 2 };
+
+struct Geom {
+    int N;       // sequence length (queries == keys)
+    int win_l;   // -1 = unbounded
+    int win_r;   // -1 = unbounded
+};
+
+// Key-tile range [lo, hi) that rows [r0, r1) (r0 < r1 <= N) must visit.
+FA_HD void kv_tile_range(const Geom& g, int r0, int r1, int& lo, int& hi) {
+    int kmin = g.win_l < 0 ? 0 : r0 - g.win_l;
+    if (kmin < 0) kmin = 0;
+    long long kmax = g.win_r < 0 ? (long long)g.N - 1 : (long long)(r1 - 1) + g.win_r;
+    if (kmax > g.N - 1) kmax = g.N - 1;
+    lo = kmin / kTileN;
+    hi = (int)(kmax / kTileN) + 1;
+}
+
+// True if key tile j (keys [j*kTileN, +kTileN)) holds a masked element for
+// some row of [r0, r0 + kTileM): ragged tail, left or right band edge.
+FA_HD bool tile_needs_mask(const Geom& g, int r0, int j) {
+    long long k0 = (long long)j * kTileN;
+    if (k0 + kTileN > g.N) return true;
+    if (g.win_l >= 0 && k0 < (long long)r0 + (kTileM - 1) - g.win_l) return true;
+    if (g.win_r >= 0 && k0 + (kTileN - 1) > (long long)r0 + g.win_r) return true;
+    return false;
+}
+
+// Visible column interval [c_lo, c_hi] (tile-local, may be empty) of query row i
+// inside key tile j.
+FA_HD void row_visible_cols(const Geom& g, int i, int j, int& c_lo, int& c_hi) {
+    long long k0 = (long long)j * kTileN;
+    long long lo = g.win_l < 0 ? 0 : (long long)i - g.win_l - k0;
+    long long hi = g.win_r < 0 ? (long long)kTileN - 1 : (long long)i + g.win_r - k0;
+    long long tail = (long long)g.N - 1 - k0;
+    if (hi > tail) hi = tail;
+    if (lo < 0) lo = 0;
+    if (hi > kTileN - 1) hi = kTileN - 1;
+    c_lo = (int)(lo > kTileN ? kTileN : lo);
+    c_hi = (int)(hi < -1 ? -1 : hi);
+}
+
+// Fewest visible keys over rows [r0, r1) (r0 < r1 <= N).  The count per row,
+// min(N-1, i+win_r) - max(0, i-win_l) + 1, is concave in i, so the minimum
+// sits at one end of the range.
+FA_HD long long min_visible_keys(const Geom& g, int r0, int r1) {
+    long long best = -1;
+    const int ends[2] = {r0, r1 - 1};
+    for (int e = 0; e < 2; ++e) {
+        const long long i = ends[e];
+        long long lo = g.win_l < 0 ? 0 : i - g.win_l;
+        if (lo < 0) lo = 0;
+        long long hi = g.win_r < 0 ? (long long)g.N - 1 : i + g.win_r;
+        if (hi > g.N - 1) hi = g.N - 1;
+        const long long c = hi - lo + 1;
+        if (best < 0 || c < best) best = c;
+    }
+    return best;
+}
+
+// Rows that see fewer keys than this carry the bf16 probabilities as an
+// unevaluated hi + lo pair (two P.V products): with few keys the 2^-9
+// relative rounding of a single bf16 P does not average out.
+constexpr int kSplitKeys = 512;
+
+FA_HD bool tile_split_p(const Geom& g, int r0) {
+    if (r0 >= g.N) return false;
+    const int r1 = r0 + kTileM < g.N ? r0 + kTileM : g.N;
+    return min_visible_keys(g, r0, r1) < kSplitKeys;
+}
+
+// One persistent work unit: two consecutive 128-row Q tiles of one (b, h).
+struct Unit {
+    int bh;      // b * H + h
+    int q0;      // first query row of tile 0
+    int lo[2];   // key-tile range per Q tile; lo == hi means the tile is empty
+    int hi[2];
+    int jlo;     // union of both ranges
+    int jhi;
+};
+
+FA_HD int n_pairs_for(int N) { return (N + 2 * kTileM - 1) / (2 * kTileM); }
+
+FA_HD Unit make_unit(const Geom& g, int BH, int order, int u) {
+    const int np = n_pairs_for(g.N);
+    int bh, pair;
+    if (order == ORDER_HEAD_MAJOR) {
+        bh = u / np;
+        pair = u % np;
+    } else if (order == ORDER_Q_DESC) {
+        pair = np - 1 - u / BH;
+        bh = u % BH;
+    } else {
+        pair = u / BH;
+        bh = u % BH;
+    }
+    Unit un;
+    un.bh = bh;
+    un.q0 = pair * 2 * kTileM;
+    un.jlo = 0x7fffffff;
+    un.jhi = 0;
+    for (int t = 0; t < 2; ++t) {
+        int r0 = un.q0 + t * kTileM;
+        if (r0 >= g.N) {
+            un.lo[t] = un.hi[t] = 0;
+            continue;
+        }
+        int r1 = r0 + kTileM < g.N ? r0 + kTileM : g.N;
+        kv_tile_range(g, r0, r1, un.lo[t], un.hi[t]);
+        if (un.lo[t] < un.jlo) un.jlo = un.lo[t];
+        if (un.hi[t] > un.jhi) un.jhi = un.hi[t];
+    }
+    return un;
+}
+
+FA_HD int unit_order_for(const Geom& g) {
+    if (g.win_r >= 0) return ORDER_Q_DESC;   // causal-like: later rows see more keys
+    if (g.win_l >= 0) return ORDER_Q_ASC;    // earlier rows see more keys
+    return ORDER_HEAD_MAJOR;                 // uniform work: keep one head's K/V hot in L2
+}
+
+}  // namespace fa

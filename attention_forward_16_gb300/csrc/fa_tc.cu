@@ -1,0 +1,565 @@
+// Tensor-core fused attention forward for sm_103a (fp16 / bf16 in, fp32 accumulate).
+//
+// The method is the tiled, online-softmax attention forward of
+// "Ascend C advanced practice: high-performance FlashAttention-2-style
+// tile-level fused attention" (section 1.2: running row max m and row sum l,
+// one division at the end; section 3: Q row blocks outer, K/V blocks inner,
+// scores kept on chip) and of the ops-transformer walk-through (section
+// "online softmax: incremental update").  The Cube/Vector pipelining of
+// "FlashAttention extreme optimisation on Ascend NPUs" (optimisation three:
+// matrix unit on block i while the vector unit does the softmax of block
+// i-1) and the double-buffered loads of its optimisation two become, on
+// Blackwell, warp specialisation around tcgen05 + TMEM + TMA:
+//
+//   warps 0-3   Q tile 0: softmax (thread = one query row), then its epilogue
+//   warps 4-7   Q tile 1: same
+//   warp  8     TMEM allocator; one thread issues every tcgen05.mma
+//   warp  9     one thread issues every TMA load (Q tiles, K/V ring)
+//
+// Ten warps put at most three on each SM sub-partition, so every thread can
+// hold 168 registers (the softmax keeps a 128-score row in registers).
+//
+// TMEM (512 columns x 128 lanes x 32 bit): S0 | S1 | O0 | O1.  P (16-bit)
+// overwrites the first half of its S columns and feeds the P.V MMA straight
+// from TMEM.  The two softmax warpgroups ping-pong: while one turns S into P,
+// the tensor core runs the other tile's MMAs.  MMA issue order per key tile
+// j: PV0(j), S0(j+1), PV1(j), S1(j+1), so each softmax has two MMA blocks of
+// slack between its S landing and its P being needed.
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records a
+// timeout in the device status word, lets its in-flight copies and MMAs
+// finish, frees TMEM and returns.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;
+constexpr int kMaxRegs = 168;     // 3 warps x 32 x 168 <= 16384 registers per sub-partition
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
+constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct TcCfg {
+    static constexpr int kChunks = D / 64;                // 128-byte column chunks per row
+    static constexpr int kBoxBytes = kTileM * 64 * 2;     // one TMA box: 128 rows x 64 elements
+    static constexpr int kTileBytes = kChunks * kBoxBytes;
+    static constexpr int kStages = D == 128 ? 4 : 8;      // K/V ring slots
+    static constexpr int kColS0 = 0;
+    static constexpr int kColS1 = 128;
+    static constexpr int kColO0 = 256;
+    static constexpr int kColO1 = 256 + D;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kTileSmem = (2 + kStages) * kTileBytes;
+};
+
+struct __align__(16) SharedCtl {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+constexpr int smem_bytes() {
+    return TcCfg<D>::kTileSmem + (int)sizeof(SharedCtl) + 1024;
+}
+
+static_assert(smem_bytes<128>() <= 227 * 1024, "shared memory budget (D=128)");
+static_assert(smem_bytes<64>() <= 227 * 1024, "shared memory budget (D=64)");
+
+// Instruction descriptor for tcgen05.mma .kind::f16 (PTX ISA, "Instruction
+// descriptor"): fp32 accumulator, A/B fp16 or bf16, A K-major, B K- or MN-major.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N, bool b_mn_major) {
+    return (1u << 4)                                  // D format: f32
+           | ((bf16 ? 1u : 0u) << 7)                  // A format
+           | ((bf16 ? 1u : 0u) << 10)                 // B format
+           | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+           | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
+// Shared-memory matrix descriptor (PTX ISA, "Shared memory descriptor"):
+// 128-byte swizzle, byte offsets given unencoded.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;   // descriptor version
+    d |= (uint64_t)2 << 61;   // SWIZZLE_128B
+    return d;
+}
+
+struct Waiter {
+    volatile int* abort;
+    int* status;
+    unsigned long long limit;
+
+    // Bounded wait on one phase.  False on timeout (recorded) or if another
+    // role already aborted.
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((it & 15u) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > limit) {
+                    *abort = 1;
+                    atomicExch(status, DEV_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+    // Warp-uniform variant: every lane waits, all lanes agree on the result.
+    __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) const {
+        bool ok = wait(bar, parity);
+        return __all_sync(0xffffffffu, ok);
+    }
+    // Bounded wait that ignores the abort flag: lets in-flight async work land
+    // before the CTA releases its resources.
+    __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (globaltimer_ns() - t0 > limit) {
+                atomicExch(status, DEV_TIMEOUT);
+                return;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return kBf16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// The two 16-bit values of a packed word, as fp32.
+template <bool kBf16>
+__device__ __forceinline__ float lo_half(uint32_t w) {
+    if (kBf16) return u2f(w << 16);
+    float f;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, a;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+}
+template <bool kBf16>
+__device__ __forceinline__ float hi_half(uint32_t w) {
+    if (kBf16) return u2f(w & 0xFFFF0000u);
+    float f;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, b;\n\t}" : "=f"(f) : "r"(w));
+    return f;
+}
+
+// ------------------------------------------------------------- TMA producer
+template <int D>
+__device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
+                                         uint32_t sKVa) {
+    using C = TcCfg<D>;
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    const uint32_t q_full = smem_u32(&sh->q_full);
+    const uint32_t q_empty = smem_u32(&sh->q_empty);
+    uint32_t kv_it = 0, q_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const Unit un = make_unit(p.g, p.BH, p.order, u);
+        if (q_it > 0 && !(ok = W.wait(q_empty, (q_it - 1) & 1))) break;
+        mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
+        for (int t = 0; t < 2; ++t)
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c * 64, un.q0 + t * kTileM,
+                            un.bh);
+        ++q_it;
+        for (int j = un.jlo; j < un.jhi && ok; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+                const int slot = kv_it % C::kStages;
+                if (kv_it >= (uint32_t)C::kStages &&
+                    !(ok = W.wait(smem_u32(&sh->kv_empty[slot]), ((kv_it / C::kStages) - 1) & 1)))
+                    break;
+                const uint32_t full = smem_u32(&sh->kv_full[slot]);
+                mbar_arrive_expect_tx(full, C::kTileBytes);
+                const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c * 64, j * kTileN, un.bh);
+                ++kv_it;
+            }
+        }
+    }
+    if (!ok) {
+        // Let every issued copy land before shared memory is released.
+        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_it; ++s) {
+            const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::kStages);
+            W.drain(smem_u32(&sh->kv_full[s]), (last / C::kStages) & 1);
+        }
+        if (q_it > 0) W.drain(q_full, (q_it - 1) & 1);
+    }
+}
+
+// --------------------------------------------------------------- MMA issuer
+template <int D, bool kBf16>
+__device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
+                                         uint32_t sKVa, uint32_t tmem) {
+    using C = TcCfg<D>;
+    constexpr uint32_t idesc_s = make_idesc(kBf16, kTileM, kTileN, false);
+    constexpr uint32_t idesc_o = make_idesc(kBf16, kTileM, D, true);
+    uint32_t kv_it = 0, q_it = 0;
+    uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+    bool ok = true;
+
+    // S_t = Q_t K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
+    auto issue_s = [&](int t, int slot) {
+        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+            const uint64_t a = make_sdesc(sQa + t * C::kTileBytes + off, 16, 1024);
+            const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + off, 16, 1024);
+            mma_ss(d, a, b, idesc_s, kk > 0);
+        }
+        mma_commit(smem_u32(&sh->s_full[t]));
+    };
+    // O_t += P_t V: P from TMEM (8 columns = 16 keys per step), V MN-major in
+    // shared memory (16 keys = two 8-row swizzle atoms = 2048 bytes per step;
+    // the second 64-column chunk of V sits one box further on).
+    // With a split P the low halves (64 columns further on) add a second product.
+    auto issue_pv = [&](int t, int slot, bool first, bool split) {
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
+            mma_ts(d, a + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+        }
+        if (split) {
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk) {
+                const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
+                mma_ts(d, a + 64 + kk * 8, b, idesc_o, 1u);
+            }
+        }
+    };
+    auto wait_kv = [&](uint32_t idx) {
+        const bool r = W.wait(smem_u32(&sh->kv_full[idx % C::kStages]), (idx / C::kStages) & 1);
+        tc_fence_after();
+        return r;
+    };
+
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const Unit un = make_unit(p.g, p.BH, p.order, u);
+        if (!(ok = W.wait(smem_u32(&sh->q_full), q_it & 1))) break;
+        ++q_it;
+        tc_fence_after();
+        const uint32_t kbase = kv_it;  // ring index of K_jlo; V_j follows K_j
+        kv_it += 2 * (un.jhi - un.jlo);
+        auto active = [&](int t, int j) { return j >= un.lo[t] && j < un.hi[t]; };
+        const bool split0 = kBf16 && tile_split_p(p.g, un.q0);
+        const bool split1 = kBf16 && tile_split_p(p.g, un.q0 + kTileM);
+
+        if (!(ok = wait_kv(kbase))) break;
+        for (int t = 0; t < 2; ++t)
+            if (active(t, un.jlo)) issue_s(t, kbase % C::kStages);
+        mma_commit(smem_u32(&sh->kv_empty[kbase % C::kStages]));
+
+        for (int j = un.jlo; j < un.jhi && ok; ++j) {
+            const uint32_t vidx = kbase + 2 * (j - un.jlo) + 1;
+            const uint32_t kidx = vidx + 1;
+            const bool has_next = j + 1 < un.jhi;
+            if (!has_next) mma_commit(smem_u32(&sh->q_empty));  // every S of this unit is issued
+            if (!(ok = wait_kv(vidx))) break;
+            bool k_ready = false;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (active(t, j)) {
+                    if (!(ok = W.wait(smem_u32(&sh->p_full[t]), p_cnt[t] & 1))) break;
+                    ++p_cnt[t];
+                    const bool first = j == un.lo[t];
+                    if (first && o_cnt[t] > 0 && !(ok = W.wait(smem_u32(&sh->o_free[t]), (o_cnt[t] - 1) & 1)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(t, vidx % C::kStages, first, t ? split1 : split0);
+                    if (j == un.hi[t] - 1) {
+                        mma_commit(smem_u32(&sh->o_done[t]));
+                        ++o_cnt[t];
+                    }
+                }
+                if (has_next && active(t, j + 1)) {
+                    if (!k_ready) {
+                        if (!(ok = wait_kv(kidx))) break;
+                        k_ready = true;
+                    }
+                    issue_s(t, kidx % C::kStages);
+                }
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&sh->kv_empty[vidx % C::kStages]));
+            if (has_next) {
+                if (!k_ready && !(ok = wait_kv(kidx))) break;
+                mma_commit(smem_u32(&sh->kv_empty[kidx % C::kStages]));
+            }
+        }
+    }
+    // Every issued MMA must complete before TMEM is released.
+    mma_commit(smem_u32(&sh->drain));
+    W.drain(smem_u32(&sh->drain), 0);
+}
+
+// ------------------------------------------------------ softmax + epilogue
+template <int D, bool kBf16, bool kPosScale>
+__device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t tmem,
+                                             int warp, int lane) {
+    using C = TcCfg<D>;
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (t ? C::kColS1 : C::kColS0);
+    const uint32_t tO = tmem + lane_base + (t ? C::kColO1 : C::kColO0);
+    const uint32_t s_full = smem_u32(&sh->s_full[t]);
+    const uint32_t p_full = smem_u32(&sh->p_full[t]);
+    const uint32_t o_done = smem_u32(&sh->o_done[t]);
+    const uint32_t o_free = smem_u32(&sh->o_free[t]);
+    const float c2 = p.scale_log2;
+    uint32_t s_cnt = 0, u_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const Unit un = make_unit(p.g, p.BH, p.order, u);
+        if (un.lo[t] == un.hi[t]) continue;
+        const int r0 = un.q0 + t * kTileM;
+        const int qi = r0 + row;
+        const bool split = kBf16 && tile_split_p(p.g, r0);
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        for (int j = un.lo[t]; j < un.hi[t]; ++j) {
+            if (!(ok = W.wait_warp(s_full, s_cnt & 1))) break;
+            ++s_cnt;
+            tc_fence_after();
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+            tmem_wait_ld();
+
+            if (!kPosScale) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c][i] = f2u(u2f(s[c][i]) * c2);
+            }
+            if (tile_needs_mask(p.g, r0, j)) {
+                int c_lo, c_hi;
+                row_visible_cols(p.g, qi, j, c_lo, c_hi);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = c * 32 + i;
+                        if (col < c_lo || col > c_hi) s[c][i] = f2u(-INFINITY);
+                    }
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    mx0 = fmaxf(mx0, u2f(s[c][i]));
+                    mx1 = fmaxf(mx1, u2f(s[c][i + 1]));
+                }
+            const float mx = fmaxf(mx0, mx1);
+            const float m_new = kPosScale ? mx * c2 : mx;
+
+            const bool first = j == un.lo[t];
+            float alpha = 1.f;
+            bool resc = false;
+            if (first) {
+                m_ref = m_new;
+            } else if (m_new > m_ref + kTau) {
+                alpha = ex2(m_ref - m_new);
+                m_ref = m_new;
+                resc = true;
+            }
+            l *= alpha;
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+            float l0 = 0.f, l1 = 0.f;
+            if (!split) {
+                uint32_t pk[2][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float a = kPosScale ? ex2(fmaf(u2f(s[c][i]), c2, neg_m)) : ex2(u2f(s[c][i]) + neg_m);
+                        const float b =
+                            kPosScale ? ex2(fmaf(u2f(s[c][i + 1]), c2, neg_m)) : ex2(u2f(s[c][i + 1]) + neg_m);
+                        pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack2<kBf16>(a, b);
+                        l0 += a;
+                        l1 += b;
+                    }
+                tmem_st32(tS, pk[0]);
+                tmem_st32(tS + 32, pk[1]);
+            } else {
+                // p = hi + lo, both bf16: hi in columns [0, 64), lo in [64, 128).
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float a = kPosScale ? ex2(fmaf(u2f(s[c][i]), c2, neg_m)) : ex2(u2f(s[c][i]) + neg_m);
+                        const float b =
+                            kPosScale ? ex2(fmaf(u2f(s[c][i + 1]), c2, neg_m)) : ex2(u2f(s[c][i + 1]) + neg_m);
+                        const uint32_t w = pack2<kBf16>(a, b);
+                        hw[i >> 1] = w;
+                        lw[i >> 1] = pack2<kBf16>(a - lo_half<kBf16>(w), b - hi_half<kBf16>(w));
+                        l0 += a;
+                        l1 += b;
+                    }
+                    tmem_st16(tS + c * 16, hw);
+                    tmem_st16(tS + 64 + c * 16, lw);
+                }
+            }
+            if (!first && __any_sync(0xffffffffu, resc)) {
+                // Rare: the running max moved by more than kTau; rescale this row of O.
+                // O is stable here: the MMA that wrote it completed before S_j did, and
+                // the next P.V waits for this warpgroup's arrival below.
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                    tmem_st32(tO + c * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full);
+            l += l0 + l1;
+        }
+        if (!ok) break;
+
+        // Epilogue: O / l, LSE = ln 2 * (m + log2 l), once the last P.V landed.
+        if (!(ok = W.wait_warp(o_done, u_cnt & 1))) break;
+        ++u_cnt;
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const bool live = qi < p.g.N;
+        const size_t orow = (size_t)un.bh * p.g.N + (size_t)(live ? qi : 0);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_wait_ld();
+            if (live) {
+                if (p.o_f32) {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv, u2f(o[4 * i + 2]) * inv,
+                                             u2f(o[4 * i + 3]) * inv);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack2<kBf16>(u2f(o[8 * i]) * inv, u2f(o[8 * i + 1]) * inv),
+                                            pack2<kBf16>(u2f(o[8 * i + 2]) * inv, u2f(o[8 * i + 3]) * inv),
+                                            pack2<kBf16>(u2f(o[8 * i + 4]) * inv, u2f(o[8 * i + 5]) * inv),
+                                            pack2<kBf16>(u2f(o[8 * i + 6]) * inv, u2f(o[8 * i + 7]) * inv));
+                }
+            }
+        }
+        if (live && p.lse) p.lse[orow] = (m_ref + log2f(l)) * kLn2;
+        tc_fence_before();
+        mbar_arrive(o_free);
+    }
+}
+
+template <int D, bool kBf16, bool kPosScale>
+__global__ void __maxnreg__(kMaxRegs) fa_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+    using C = TcCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SharedCtl* sh = reinterpret_cast<SharedCtl*>(smem + C::kTileSmem);
+    const uint32_t sQa = smem_u32(smem);
+    const uint32_t sKVa = sQa + 2 * C::kTileBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&sh->q_full), 1);
+        mbar_init(smem_u32(&sh->q_empty), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&sh->kv_full[s]), 1);
+            mbar_init(smem_u32(&sh->kv_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&sh->s_full[t]), 1);
+            mbar_init(smem_u32(&sh->p_full[t]), 128);
+            mbar_init(smem_u32(&sh->o_done[t]), 1);
+            mbar_init(smem_u32(&sh->o_free[t]), 128);
+        }
+        mbar_init(smem_u32(&sh->drain), 1);
+        sh->abort = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
+
+    if (warp < 8) {
+        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, warp, lane);
+    } else if (warp == kWarpMma) {
+        if (lane == 0) mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem);
+    } else if (warp == kWarpTma) {
+        if (lane == 0) tma_role<D>(p, W, sh, sQa, sKVa);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool kBf16, bool kPos>
+cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
+    auto kern = fa_fwd_tc_kernel<D, kBf16, kPos>;
+    constexpr int smem = smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s) {
+    if (D == 128) {
+        if (bf16) return pos_scale ? launch_one<128, true, true>(p, grid, s) : launch_one<128, true, false>(p, grid, s);
+        return pos_scale ? launch_one<128, false, true>(p, grid, s) : launch_one<128, false, false>(p, grid, s);
+    }
+    if (bf16) return pos_scale ? launch_one<64, true, true>(p, grid, s) : launch_one<64, true, false>(p, grid, s);
+    return pos_scale ? launch_one<64, false, true>(p, grid, s) : launch_one<64, false, false>(p, grid, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,387 @@
+"""Benchmark: fused attention forward TFLOP/s on one GB300 (or N replicas).
+
+One step = one fused attention forward over the whole batch of the
+benchmark workload (default: B=4, H=32, N=4096, D=128, fp16, no mask -- the
+pages' benchmark shape, "FlashAttention under the catlass template",
+section "Performance data").  Inputs are seeded synthetic tensors resident
+in HBM before the timed region; their 512 MiB working set (Q, K, V, O)
+exceeds the 126 MB L2, so no extra flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the float64 CPU
+oracle on a bounded sample of the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       [--impl reference]
+Multi-GPU: torchrun --nproc-per-node N bench.py --gpus N ...  (independent
+replicas, one per GPU: the (b, h) problems are independent, so there is no
+data exchange; timing is reduced with a max over ranks).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused attention fwd TFLOP/s and % of GB300 dense FP16 tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="f16_full_4k")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": FALLBACK_PEAK_TFLOPS}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+        self.mark = len(self.lines)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = [r.split(", ") for r in self.lines[self.mark:] if r.count(",") >= 8] or \
+               [r.split(", ") for r in self.lines if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "native" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def reduce_max(pg, x, device):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg, device):
+    if pg is not None:
+        import torch
+        pg.barrier(device_ids=[device.index]) if device.type == "cuda" else pg.barrier()
+
+
+# ---------------------------------------------------------- reference arm
+
+def cpu_oracle_sample(w, q, k, v, budget_s, rows=None):
+    """Time the oracle, as it stands, on (b, h) heads of the workload until
+    `budget_s` seconds pass; returns (TFLOP/s, description, cores)."""
+    import numpy as np
+    from oracle import attention_three_pass
+    from attention_forward_16_gb300.flops import visible_keys_per_row
+    qd, kd, vd = (t.float().numpy() for t in (q, k, v))
+    per_row = visible_keys_per_row(w.N, w.mask, w.win_l, w.win_r)
+    done_flops, heads, t_total = 0, 0, 0.0
+    r = rows or w.N
+    while t_total < budget_s and heads < w.B * w.H:
+        b, h = divmod(heads, w.H)
+        r0 = (heads * 977) % max(1, w.N - r + 1) if rows else 0
+        t0 = time.perf_counter()
+        attention_three_pass(qd[b:b + 1, h:h + 1, r0:r0 + r], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                             w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
+        t_total += time.perf_counter() - t0
+        done_flops += 4 * w.D * int(per_row[r0:r0 + r].sum())
+        heads += 1
+    desc = f"{heads} of {w.B * w.H} heads" + (f", {r} query rows each" if rows else ", all rows") + \
+        f" of {w.name}, float64 numpy, {t_total:.1f} s"
+    return done_flops / t_total / 1e12, desc, blas_threads()
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return 0
+    from attention_forward_16_gb300.inputs import make_workload
+    q, k, v = make_workload(w)
+    import numpy as np
+    from oracle import attention_three_pass
+    from attention_forward_16_gb300.flops import visible_keys_per_row
+    per_row = visible_keys_per_row(w.N, w.mask, w.win_l, w.win_r)
+    qd, kd, vd = (t.float().numpy() for t in (q, k, v))
+    rows = 64
+
+    def step(i):
+        b, h = divmod(i % (w.B * w.H), w.H)
+        r0 = (i * 977) % (w.N - rows + 1)
+        attention_three_pass(qd[b:b + 1, h:h + 1, r0:r0 + rows], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                             w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
+        return 4 * w.D * int(per_row[r0:r0 + rows].sum())
+
+    for i in range(args.warmup):
+        step(i)
+    flops_total = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops_total += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops_total / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype_in": w.dtype,
+                   "mask": w.mask, "window": [w.win_l, w.win_r], "step": f"{rows} query rows of one head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"{rows} query rows x full keys of one (b, h) per step, float64 numpy"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- native arm
+
+def run_native(args, w, world, rank, local, pg):
+    import torch
+    import attention_forward_16_gb300 as fa
+    from attention_forward_16_gb300.build import build
+    from attention_forward_16_gb300.flops import algorithmic_bytes, attention_flops
+    from attention_forward_16_gb300.inputs import make_workload
+
+    build()
+    fa.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    q, k, v = make_workload(w)
+    dq, dk, dv = q.to(device), k.to(device), v.to(device)
+    do = torch.empty_like(dq)
+    dl = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
+    causal = w.mask == fa.FA_MASK_CAUSAL
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.attention_fwd(dq, dk, dv, scale=w.scale, causal=causal, window=window, out=do, lse=dl)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+
+    clocks = ClockSampler(local).start() if rank == 0 else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(pg, device)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    clk = clocks.stop() if clocks else None
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("kernel reported a timeout during the timed steps")
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = reduce_max(pg, total_ms, device)
+    avg_launch_ms = reduce_max(pg, sum(launch_ms) / len(launch_ms), device)
+
+    flops_step = attention_flops(w.B, w.H, w.N, w.D, w.mask, w.win_l, w.win_r)
+    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+
+    # ------------------------------------------------ end to end (host buffers)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+    hl = torch.empty(dl.shape, dtype=dl.dtype, pin_memory=True)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.attention_fwd(dq, dk, dv, scale=w.scale, causal=causal, window=window, out=do, lse=dl)
+        ho.copy_(do, non_blocking=True)
+        hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(pg, e0.elapsed_time(e1), device)
+    e2e_value = flops_step * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "mask": w.mask,
+                   "window": [w.win_l, w.win_r], "scale": w.scale, "global_batch": w.B * world,
+                   "seq_len": w.N, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "working set (Q,K,V,O = %d MiB) exceeds L2; no flush" % (
+                       algorithmic_bytes(w.B, w.H, w.N, w.D, w.dtype) >> 20),
+                   "pct_of_peak": round(100.0 * value / world / peak, 2), "peak_tflops": peak,
+                   "peak_source": f"{peak_src} bf16 burst (fp16 dense rate is the same)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "fa_fwd_tc_kernel<%d,%s>" % (w.D, w.dtype),
+                     "algorithmic_flops_per_launch": flops_step,
+                     "avg_launch_ms": avg_launch_ms, "peak_source": peak_src},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tf, desc, cores = cpu_oracle_sample(w, q, k, v, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from attention_forward_16_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world, rank, local, pg = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, world, rank)
+        return run_native(args, w, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * libfa -- fused attention forward for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * Computes, for every batch b and head h,
+ *
+ *     S   = scale * Q K^T              (scores, never written to memory)
+ *     S_ij = -inf where the mask hides key j from query i
+ *     O   = softmax_rows(S) V
+ *     LSE_i = ln sum_j exp(S_ij)       (natural log, fp32)
+ *
+ * Definition: "Ascend C advanced practice: high-performance
+ * FlashAttention-2-style tile-level fused attention", section 1.1 (the MHA
+ * definition) and section 1.2 (the online-softmax identity the kernels use);
+ * the causal rule follows its section 4.2 kernel (a key after the query is
+ * masked); the (window_left, window_right) sliding window follows "FlashAttention
+ * under the catlass template", section "Usage" (full / causal / window masks
+ * handled by one kernel), read as the inclusive band i - win_l <= j <= i + win_r.
+ *
+ * Layout: Q, K, V and O are contiguous [B, H, N, D] row-major tensors (D is
+ * the fastest axis), as in the ops-transformer walk-through's aclnn call
+ * ({B, H, S, D} ND tensors).  LSE is a contiguous [B, H, N] fp32 tensor.
+ *
+ * Ownership: every pointer is caller-owned CUDA device memory; the library
+ * allocates nothing and keeps no reference after the kernel finishes.
+ * Pointers must be 16-byte aligned.  O must not alias Q, K or V.
+ *
+ * Asynchrony: a return of FA_OK means the work was enqueued on `stream`
+ * (a cudaStream_t, or 0 for the legacy default stream).  Kernel-side
+ * failures (a bounded wait that timed out) are reported through
+ * fa_device_status().
+ *
+ * Thread safety: the entry points may be called from several host threads
+ * on different streams.  The only global state is one device status word
+ * (see fa_device_status) and a per-device cache of the SM count.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Mask kinds. CAUSAL == WINDOW(-1, 0); NONE == WINDOW(-1, -1). */
+enum {
+    FA_MASK_NONE = 0,    /* every key visible                                  */
+    FA_MASK_CAUSAL = 1,  /* key j visible to query i iff j <= i                */
+    FA_MASK_WINDOW = 2   /* visible iff i - win_l <= j <= i + win_r; a bound of
+                            -1 means unbounded on that side                    */
+};
+
+/* Element types of Q, K, V (and O unless fa_fwd_ex overrides it). */
+enum { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2 };
+
+/* Return codes. Negative codes mean nothing was launched. */
+enum {
+    FA_OK = 0,
+    FA_ERR_ARG = -1,          /* null pointer, B/H/N <= 0, non-finite scale,
+                                 window bound < -1, unknown mask kind, or a
+                                 size whose element count overflows 2^62       */
+    FA_ERR_UNSUPPORTED = -2,  /* f16/bf16 need D in {64, 128}; f32 needs
+                                 1 <= D <= 128; unknown dtype                  */
+    FA_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned              */
+    FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed; see
+                                 fa_last_cuda_error()                          */
+    FA_ERR_TIMEOUT = -5,      /* (fa_device_status) a kernel wait timed out    */
+    FA_ERR_DEVICE = -6        /* (fa_device_status) the stream reported a CUDA
+                                 error                                         */
+};
+
+/*
+ * fa_fwd -- fused attention forward, O and LSE from Q, K, V.
+ *
+ *   q, k, v   [B, H, N, D] device pointers of element type `dtype`.
+ *   o         [B, H, N, D] device pointer, same element type as q.
+ *   lse       [B, H, N] fp32 device pointer, or NULL to skip it.
+ *   B, H, N   batch, heads, sequence length (queries == keys == N), all >= 1.
+ *   D         head dimension (see FA_ERR_UNSUPPORTED).
+ *   scale     multiplies Q K^T before masking; any finite value (0 is legal:
+ *             every visible key then gets equal weight).
+ *   mask_kind FA_MASK_NONE / FA_MASK_CAUSAL / FA_MASK_WINDOW.
+ *   win_l, win_r  window bounds (>= -1), read only for FA_MASK_WINDOW.
+ *   dtype     FA_F16 / FA_BF16 (tensor-core kernel) or FA_F32 (fp32 FFMA kernel).
+ *   stream    cudaStream_t to enqueue on.
+ *
+ * Accumulation is fp32 throughout; for 16-bit inputs the softmax
+ * probabilities are rounded to the input type before the P.V product.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int D, float scale,
+           int mask_kind, int win_l, int win_r, int dtype, void* stream);
+
+/* Typed conveniences with exactly the argument list of the method's call:
+ * fa_fwd(q,k,v,o,lse,B,H,N,D,scale,mask_kind,win_l,win_r,stream). */
+int fa_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int N, int D, float scale,
+               int mask_kind, int win_l, int win_r, void* stream);
+int fa_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int N, int D, float scale,
+                int mask_kind, int win_l, int win_r, void* stream);
+int fa_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int N, int D, float scale,
+               int mask_kind, int win_l, int win_r, void* stream);
+
+/*
+ * fa_fwd_ex -- as fa_fwd, but O is written with element type `o_dtype`
+ * (FA_F32 lets a caller see the fp32 accumulator divided by the row sum
+ * before any 16-bit output rounding; otherwise o_dtype must equal dtype).
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int N, int D, float scale,
+              int mask_kind, int win_l, int win_r, int dtype, int o_dtype,
+              void* stream);
+
+/*
+ * fa_device_status -- synchronise `stream`, then report and clear the
+ * library's device status word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel
+ * wait ran past its limit; the kernel stopped early and its outputs are
+ * undefined) or FA_ERR_DEVICE (the stream synchronisation itself failed).
+ */
+int fa_device_status(void* stream);
+
+/* Wait limit, in nanoseconds, for every bounded wait inside the kernels of
+ * this device (default 2e9).  Returns the previous value. */
+unsigned long long fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * fa_selftest_wait_timeout -- enqueue a one-CTA kernel that waits on an
+ * mbarrier nothing ever arrives at, bounded by `limit_ns`; it records
+ * FA_ERR_TIMEOUT in the device status word and returns.  Exists so a test
+ * can check the watchdog path without touching the attention kernels.
+ */
+int fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/*
+ * fa_plan_units -- host-side view of the work decomposition the tensor-core
+ * kernel uses (no GPU needed).  Units are pairs of 128-row query tiles of one
+ * (b, h), in the order persistent CTAs take them.  If `out` is not NULL,
+ * writes min(cap, n_units) records of 6 ints {bh, q0, lo0, hi0, lo1, hi1}:
+ * query rows [q0, q0+128) visit key tiles [lo0, hi0), rows [q0+128, q0+256)
+ * visit [lo1, hi1) (key tile j = keys [128 j, 128 j + 128)); lo == hi marks a
+ * tile past the end of the sequence.  Returns n_units or FA_ERR_ARG.
+ */
+int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int* out, int cap);
+
+/* 1 if key tile j holds a masked element for some row of the 128-row query
+ * tile starting at r0 (the kernel then applies per-element masks), 0 if the
+ * whole tile is visible, FA_ERR_ARG on a bad mask.  No GPU needed. */
+int fa_tile_needs_mask(int N, int mask_kind, int win_l, int win_r, int r0, int j);
+
+/* Human-readable text for a return code. Never NULL. */
+const char* fa_strerror(int code);
+
+/* The CUDA error string of the last FA_ERR_CUDA on this host thread. */
+const char* fa_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

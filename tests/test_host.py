@@ -1,0 +1,161 @@
+"""Host-side checks that need no GPU: the library builds, loads and exports
+every symbol of include/fa.h; argument validation; the tile planner and the
+mask-free-tile predicate against the oracle's mask; the FLOP count against
+the oracle's pair count."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from attention_forward_16_gb300 import binding as fb
+from attention_forward_16_gb300 import flops
+from oracle import MASK_CAUSAL, MASK_NONE, MASK_WINDOW, allowed_mask, unmasked_pairs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_16_gb300.build import build
+    build()
+    return fb.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_ ]+\**\s*\**(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_method_entry_points():
+    names = _declared_functions()
+    for n in ("fa_fwd", "fa_fwd_f16", "fa_fwd_bf16", "fa_fwd_f32", "fa_fwd_ex", "fa_device_status",
+              "fa_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"libfa.so does not export {n}"
+    assert set(names) == set(fb.SIGNATURES), "binding signatures out of sync with include/fa.h"
+
+
+def test_version_and_strerror(lib):
+    assert lib.fa_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5, -6, 7):
+        assert lib.fa_strerror(code)
+
+
+# ----------------------------------------------------- validation, no launch
+
+def _call(lib, q=16, k=16, v=16, o=16, lse=None, B=1, H=1, N=8, D=64, scale=0.1, mk=0, wl=-1, wr=-1, dt=0, odt=None):
+    return lib.fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mk, wl, wr, dt, dt if odt is None else odt, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fb.FA_ERR_ARG),
+    (dict(o=None), fb.FA_ERR_ARG),
+    (dict(B=0), fb.FA_ERR_ARG),
+    (dict(H=-1), fb.FA_ERR_ARG),
+    (dict(N=0), fb.FA_ERR_ARG),
+    (dict(scale=float("nan")), fb.FA_ERR_ARG),
+    (dict(scale=float("inf")), fb.FA_ERR_ARG),
+    (dict(mk=3), fb.FA_ERR_ARG),
+    (dict(mk=2, wl=-2), fb.FA_ERR_ARG),
+    (dict(mk=2, wr=-5), fb.FA_ERR_ARG),
+    (dict(B=1 << 20, H=1 << 12), fb.FA_ERR_ARG),
+    (dict(D=96), fb.FA_ERR_UNSUPPORTED),
+    (dict(D=256, dt=1), fb.FA_ERR_UNSUPPORTED),
+    (dict(D=129, dt=2), fb.FA_ERR_UNSUPPORTED),
+    (dict(dt=5), fb.FA_ERR_UNSUPPORTED),
+    (dict(dt=0, odt=1), fb.FA_ERR_UNSUPPORTED),
+    (dict(dt=2, odt=0), fb.FA_ERR_UNSUPPORTED),
+    (dict(q=24), fb.FA_ERR_ALIGN),
+    (dict(o=8), fb.FA_ERR_ALIGN),
+    (dict(lse=2), fb.FA_ERR_ALIGN),
+])
+def test_validation_rejects_before_any_launch(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+# ----------------------------------------------------------- tile planning
+
+PLAN_CASES = [
+    (1, 300, MASK_NONE, -1, -1),
+    (2, 513, MASK_CAUSAL, -1, -1),
+    (1, 1, MASK_CAUSAL, -1, -1),
+    (1, 129, MASK_WINDOW, 37, 5),
+    (1, 1000, MASK_WINDOW, 200, 0),
+    (1, 700, MASK_WINDOW, 0, 0),
+    (1, 640, MASK_WINDOW, -1, 3),
+    (1, 650, MASK_WINDOW, 130, -1),
+    (1, 2048, MASK_WINDOW, 1024, 0),
+]
+
+
+@pytest.mark.parametrize("BH,N,mk,wl,wr", PLAN_CASES)
+def test_plan_covers_exactly_the_visible_pairs(lib, BH, N, mk, wl, wr):
+    units = fb.fa_plan_units(1, BH, N, mk, wl, wr)
+    ok = allowed_mask(N, N, mk, wl, wr)
+    seen_rows = {}
+    for (bh, q0, lo0, hi0, lo1, hi1) in units:
+        for t, (lo, hi) in enumerate(((lo0, hi0), (lo1, hi1))):
+            r0 = q0 + 128 * t
+            if r0 >= N:
+                assert lo == hi
+                continue
+            r1 = min(N, r0 + 128)
+            assert 0 <= lo < hi <= (N + 127) // 128
+            for r in range(r0, r1):
+                seen_rows[(bh, r)] = seen_rows.get((bh, r), 0) + 1
+            rows = ok[r0:r1]
+            # every visible key of these rows lies in a visited tile ...
+            cols = np.nonzero(rows.any(axis=0))[0]
+            assert cols.min() >= lo * 128 and cols.max() < hi * 128
+            # ... and the first and last visited tiles hold at least one
+            assert rows[:, lo * 128:(lo + 1) * 128].any() and rows[:, (hi - 1) * 128:hi * 128].any()
+    assert len(seen_rows) == BH * N and set(seen_rows.values()) == {1}
+
+
+@pytest.mark.parametrize("BH,N,mk,wl,wr", PLAN_CASES)
+def test_tiles_without_mask_are_fully_visible(lib, BH, N, mk, wl, wr):
+    ok = allowed_mask(N, N, mk, wl, wr)
+    nt = (N + 127) // 128
+    for r0 in range(0, N, 128):
+        r1 = min(N, r0 + 128)
+        for j in range(nt):
+            block = ok[r0:r1, j * 128:min(N, (j + 1) * 128)]
+            need = fb.fa_tile_needs_mask(N, mk, wl, wr, r0, j)
+            assert need in (0, 1)
+            if not need:
+                assert block.all() and (j + 1) * 128 <= N
+
+
+def test_unit_order_is_longest_first_for_causal(lib):
+    units = fb.fa_plan_units(2, 3, 1024, MASK_CAUSAL)
+    work = [(hi0 - lo0) + (hi1 - lo1) for (_, _, lo0, hi0, lo1, hi1) in units]
+    assert work == sorted(work, reverse=True)
+
+
+# ------------------------------------------------------------- FLOP count
+
+@pytest.mark.parametrize("N", [1, 2, 7, 128, 129, 1000])
+@pytest.mark.parametrize("mk,wl,wr", [(MASK_NONE, -1, -1), (MASK_CAUSAL, -1, -1), (MASK_WINDOW, 5, 0),
+                                      (MASK_WINDOW, 0, 3), (MASK_WINDOW, 40, 17), (MASK_WINDOW, -1, 2),
+                                      (MASK_WINDOW, 3, -1), (MASK_WINDOW, 0, 0)])
+def test_pair_count_matches_oracle_mask(N, mk, wl, wr):
+    assert flops.unmasked_pairs(N, mk, wl, wr) == unmasked_pairs(N, mk, wl, wr)
+
+
+def test_flops_of_the_benchmark_shapes():
+    assert flops.attention_flops(4, 32, 4096, 128, MASK_NONE) == 2 ** 40
+    assert flops.attention_flops(4, 32, 4096, 128, MASK_CAUSAL) == 549_890_031_616
+    assert flops.attention_flops(1, 64, 16384, 128, MASK_WINDOW, 1024, 0) == 533_096_038_400
+    assert flops.attention_flops(2, 8, 1024, 64, MASK_CAUSAL) == 2_149_580_800
+    assert flops.algorithmic_bytes(4, 32, 4096, 128, "f16") == 538_968_064
