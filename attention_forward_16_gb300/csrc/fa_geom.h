@@ -85,7 +85,7 @@ FA_HD long long min_visible_keys(const Geom& g, int r0, int r1) {
 }
 
 // Rows that see fewer keys than this carry the bf16 probabilities as an
-// unevaluated hi + lo pair (two P.V products): with few keys the 2^-9
+// unevaluated hi + lo pair (two P.V products): with few keys the 2^-8
 // relative rounding of a single bf16 P does not average out.
 constexpr int kSplitKeys = 512;
 

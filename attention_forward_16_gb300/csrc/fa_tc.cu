@@ -15,9 +15,12 @@
 //   warps 4-7   Q tile 1: same
 //   warp  8     TMEM allocator; one thread issues every tcgen05.mma
 //   warp  9     one thread issues every TMA load (Q tiles, K/V ring)
+//   warps 10-11 idle (they complete the third warpgroup)
 //
-// Ten warps put at most three on each SM sub-partition, so every thread can
-// hold 168 registers (the softmax keeps a 128-score row in registers).
+// The launch gives 168 registers a thread (12 warps, three per SM
+// sub-partition); setmaxnreg then moves 48 from the MMA/TMA warpgroup to the
+// softmax warpgroups, so a softmax thread can hold its 128-score row
+// (192 + 192 + 120 = 3 x 168).
 //
 // TMEM (512 columns x 128 lanes x 32 bit): S0 | S1 | O0 | O1.  P (16-bit)
 // overwrites the first half of its S columns and feeds the P.V MMA straight
@@ -30,6 +33,7 @@
 // timeout in the device status word, lets its in-flight copies and MMAs
 // finish, frees TMEM and returns.
 #include <cmath>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -39,8 +43,15 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 320;
-constexpr int kMaxRegs = 168;     // 3 warps x 32 x 168 <= 16384 registers per sub-partition
+constexpr int kThreads = 384;
+// Registers a thread at launch: the 65536-entry file over 384 threads,
+// rounded down to the allocation granule of 8 (ptxas reports this count).
+constexpr int kLaunchRegs = (65536 / kThreads) & ~7;  // 168
+constexpr int kRegSoftmax = 192;  // per thread, warpgroups 0-1
+constexpr int kRegOther = 120;    // per thread, warpgroup 2 (MMA, TMA, idle)
+// setmaxnreg.inc only draws on the registers the CTA was launched with; a
+// split above that total would wait forever.
+static_assert(2 * kRegSoftmax + kRegOther <= 3 * kLaunchRegs, "register split exceeds the launch budget");
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
@@ -218,7 +229,9 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     constexpr uint32_t idesc_s = make_idesc(kBf16, kTileM, kTileN, false);
     constexpr uint32_t idesc_o = make_idesc(kBf16, kTileM, D, true);
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+    // Per-tile counters as plain scalars: a runtime index into a small array
+    // would push it to local memory.
+    uint32_t p_cnt0 = 0, p_cnt1 = 0, o_cnt0 = 0, o_cnt1 = 0;
     bool ok = true;
 
     // S_t = Q_t K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
@@ -266,13 +279,42 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         tc_fence_after();
         const uint32_t kbase = kv_it;  // ring index of K_jlo; V_j follows K_j
         kv_it += 2 * (un.jhi - un.jlo);
-        auto active = [&](int t, int j) { return j >= un.lo[t] && j < un.hi[t]; };
+        const int lo0 = un.lo[0], hi0 = un.hi[0], lo1 = un.lo[1], hi1 = un.hi[1];
         const bool split0 = kBf16 && tile_split_p(p.g, un.q0);
         const bool split1 = kBf16 && tile_split_p(p.g, un.q0 + kTileM);
 
+        // One Q tile's share of key step j: P.V for j, then S for j + 1.
+        auto tile_step = [&](auto tc, int j, uint32_t vidx, uint32_t kidx, bool has_next, bool& k_ready) -> bool {
+            constexpr int t = decltype(tc)::value;
+            const int lo = t ? lo1 : lo0;
+            const int hi = t ? hi1 : hi0;
+            uint32_t& pc = t ? p_cnt1 : p_cnt0;
+            uint32_t& oc = t ? o_cnt1 : o_cnt0;
+            if (j >= lo && j < hi) {
+                if (!W.wait(smem_u32(&sh->p_full[t]), pc & 1)) return false;
+                ++pc;
+                const bool first = j == lo;
+                if (first && oc > 0 && !W.wait(smem_u32(&sh->o_free[t]), (oc - 1) & 1)) return false;
+                tc_fence_after();
+                issue_pv(t, vidx % C::kStages, first, t ? split1 : split0);
+                if (j == hi - 1) {
+                    mma_commit(smem_u32(&sh->o_done[t]));
+                    ++oc;
+                }
+            }
+            if (has_next && j + 1 >= lo && j + 1 < hi) {
+                if (!k_ready) {
+                    if (!wait_kv(kidx)) return false;
+                    k_ready = true;
+                }
+                issue_s(t, kidx % C::kStages);
+            }
+            return true;
+        };
+
         if (!(ok = wait_kv(kbase))) break;
-        for (int t = 0; t < 2; ++t)
-            if (active(t, un.jlo)) issue_s(t, kbase % C::kStages);
+        if (un.jlo >= lo0 && un.jlo < hi0) issue_s(0, kbase % C::kStages);
+        if (un.jlo >= lo1 && un.jlo < hi1) issue_s(1, kbase % C::kStages);
         mma_commit(smem_u32(&sh->kv_empty[kbase % C::kStages]));
 
         for (int j = un.jlo; j < un.jhi && ok; ++j) {
@@ -282,28 +324,8 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
             if (!has_next) mma_commit(smem_u32(&sh->q_empty));  // every S of this unit is issued
             if (!(ok = wait_kv(vidx))) break;
             bool k_ready = false;
-            for (int t = 0; t < 2 && ok; ++t) {
-                if (active(t, j)) {
-                    if (!(ok = W.wait(smem_u32(&sh->p_full[t]), p_cnt[t] & 1))) break;
-                    ++p_cnt[t];
-                    const bool first = j == un.lo[t];
-                    if (first && o_cnt[t] > 0 && !(ok = W.wait(smem_u32(&sh->o_free[t]), (o_cnt[t] - 1) & 1)))
-                        break;
-                    tc_fence_after();
-                    issue_pv(t, vidx % C::kStages, first, t ? split1 : split0);
-                    if (j == un.hi[t] - 1) {
-                        mma_commit(smem_u32(&sh->o_done[t]));
-                        ++o_cnt[t];
-                    }
-                }
-                if (has_next && active(t, j + 1)) {
-                    if (!k_ready) {
-                        if (!(ok = wait_kv(kidx))) break;
-                        k_ready = true;
-                    }
-                    issue_s(t, kidx % C::kStages);
-                }
-            }
+            ok = tile_step(std::integral_constant<int, 0>{}, j, vidx, kidx, has_next, k_ready) &&
+                 tile_step(std::integral_constant<int, 1>{}, j, vidx, kidx, has_next, k_ready);
             if (!ok) break;
             mma_commit(smem_u32(&sh->kv_empty[vidx % C::kStages]));
             if (has_next) {
@@ -337,13 +359,15 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     bool ok = true;
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
-        if (un.lo[t] == un.hi[t]) continue;
+        const int jlo_t = t ? un.lo[1] : un.lo[0];
+        const int jhi_t = t ? un.hi[1] : un.hi[0];
+        if (jlo_t == jhi_t) continue;
         const int r0 = un.q0 + t * kTileM;
         const int qi = r0 + row;
         const bool split = kBf16 && tile_split_p(p.g, r0);
         float m_ref = -INFINITY;
         float l = 0.f;
-        for (int j = un.lo[t]; j < un.hi[t]; ++j) {
+        for (int j = jlo_t; j < jhi_t; ++j) {
             if (!(ok = W.wait_warp(s_full, s_cnt & 1))) break;
             ++s_cnt;
             tc_fence_after();
@@ -356,7 +380,12 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c][i] = f2u(u2f(s[c][i]) * c2);
+                    for (int i = 0; i < 32; i += 2) {
+                        float a, b;
+                        fmul2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), c2, c2);
+                        s[c][i] = f2u(a);
+                        s[c][i + 1] = f2u(b);
+                    }
             }
             if (tile_needs_mask(p.g, r0, j)) {
                 int c_lo, c_hi;
@@ -369,18 +398,21 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                         if (col < c_lo || col > c_hi) s[c][i] = f2u(-INFINITY);
                     }
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            // Row max: 64 three-input maxes spread over 8 independent chains.
+            float mxk[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(u2f(s[0][2 * k]), u2f(s[0][2 * k + 1]));
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    mx0 = fmaxf(mx0, u2f(s[c][i]));
-                    mx1 = fmaxf(mx1, u2f(s[c][i + 1]));
+                for (int i = (c == 0 ? 16 : 0); i < 32; i += 2) {
+                    const int k = (i >> 1) & 7;
+                    mxk[k] = max3(mxk[k], u2f(s[c][i]), u2f(s[c][i + 1]));
                 }
-            const float mx = fmaxf(mx0, mx1);
+            const float mx = fmaxf(max3(mxk[0], mxk[1], mxk[2]), max3(max3(mxk[3], mxk[4], mxk[5]), mxk[6], mxk[7]));
             const float m_new = kPosScale ? mx * c2 : mx;
 
-            const bool first = j == un.lo[t];
+            const bool first = j == jlo_t;
             float alpha = 1.f;
             bool resc = false;
             if (first) {
@@ -394,20 +426,29 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
             float l0 = 0.f, l1 = 0.f;
             if (!split) {
-                uint32_t pk[2][32];
+                // p = 2^(s*c - m) two at a time (packed FFMA, two ex2), packed into
+                // 16-bit pairs; the row sum runs over four packed accumulators.
+                float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const float a = kPosScale ? ex2(fmaf(u2f(s[c][i]), c2, neg_m)) : ex2(u2f(s[c][i]) + neg_m);
-                        const float b =
-                            kPosScale ? ex2(fmaf(u2f(s[c][i + 1]), c2, neg_m)) : ex2(u2f(s[c][i + 1]) + neg_m);
-                        pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack2<kBf16>(a, b);
-                        l0 += a;
-                        l1 += b;
+                        float a, b;
+                        if (kPosScale)
+                            ffma2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), c2, c2, neg_m, neg_m);
+                        else
+                            fadd2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), neg_m, neg_m);
+                        a = ex2(a);
+                        b = ex2(b);
+                        pk[i >> 1] = pack2<kBf16>(a, b);
+                        const int k = (i >> 1) & 3;
+                        fadd2(acc[k][0], acc[k][1], acc[k][0], acc[k][1], a, b);
                     }
-                tmem_st32(tS, pk[0]);
-                tmem_st32(tS + 32, pk[1]);
+                    tmem_st16(tS + 16 * c, pk);
+                }
+                l0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+                l1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
             } else {
                 // p = hi + lo, both bf16: hi in columns [0, 64), lo in [64, 128).
 #pragma unroll
@@ -486,7 +527,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
 }
 
 template <int D, bool kBf16, bool kPosScale>
-__global__ void __maxnreg__(kMaxRegs) fa_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = TcCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -525,6 +566,12 @@ __global__ void __maxnreg__(kMaxRegs) fa_fwd_tc_kernel(const __grid_constant__ T
     const uint32_t tmem = sh->tmem_base;
     const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
 
+    // setmaxnreg is warpgroup-wide: all four warps of a group run the same one.
+    if (warp >= 8)
+        setmaxnreg_dec<kRegOther>();
+    else
+        setmaxnreg_inc<kRegSoftmax>();
+
     if (warp < 8) {
         softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, warp, lane);
     } else if (warp == kWarpMma) {
@@ -545,7 +592,13 @@ template <int D, bool kBf16, bool kPos>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
     auto kern = fa_fwd_tc_kernel<D, kBf16, kPos>;
     constexpr int smem = smem_bytes<D>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    // Refuse to launch if the registers the CTA starts with cannot cover the
+    // setmaxnreg split (the increase would never be granted).
+    if (3 * attr.numRegs < 2 * kRegSoftmax + kRegOther) return cudaErrorLaunchOutOfResources;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();

@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="f16_full_4k")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiling)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -373,6 +375,9 @@ def main(argv=None):
     args = parse_args(argv)
     from attention_forward_16_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_b{args.batch}")
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":
