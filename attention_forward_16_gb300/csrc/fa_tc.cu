@@ -13,9 +13,10 @@
 //
 //   warps 0-3   Q tile 0: softmax (thread = one query row), then its epilogue
 //   warps 4-7   Q tile 1: same
-//   warp  8     TMEM allocator; one thread issues every tcgen05.mma
+//   warp  8     TMEM allocator; one thread issues Q tile 0's tcgen05.mma
 //   warp  9     one thread issues every TMA load (Q tiles, K/V ring)
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  10    one thread issues Q tile 1's tcgen05.mma
+//   warp  11    idle (completes the third warpgroup)
 //
 // The launch gives 168 registers a thread (12 warps, three per SM
 // sub-partition); setmaxnreg then moves 48 from the MMA/TMA warpgroup to the
@@ -25,9 +26,9 @@
 // TMEM (512 columns x 128 lanes x 32 bit): S0 | S1 | O0 | O1.  P (16-bit)
 // overwrites the first half of its S columns and feeds the P.V MMA straight
 // from TMEM.  The two softmax warpgroups ping-pong: while one turns S into P,
-// the tensor core runs the other tile's MMAs.  MMA issue order per key tile
-// j: PV0(j), S0(j+1), PV1(j), S1(j+1), so each softmax has two MMA blocks of
-// slack between its S landing and its P being needed.
+// the tensor core runs the other tile's MMAs.  Each tile has its own issuing
+// thread (order P.V(j), S(j+1) per tile), so the two tiles settle into
+// alternating on the tensor core without waiting for each other.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records a
 // timeout in the device status word, lets its in-flight copies and MMAs
@@ -52,8 +53,9 @@ constexpr int kRegOther = 120;    // per thread, warpgroup 2 (MMA, TMA, idle)
 // setmaxnreg.inc only draws on the registers the CTA was launched with; a
 // split above that total would wait forever.
 static_assert(2 * kRegSoftmax + kRegOther <= 3 * kLaunchRegs, "register split exceeds the launch budget");
-constexpr int kWarpMma = 8;
+constexpr int kWarpMma = 8;    // MMA issuer for Q tile 0; TMEM owner
 constexpr int kWarpTma = 9;
+constexpr int kWarpMma1 = 10;  // MMA issuer for Q tile 1
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -75,7 +77,8 @@ struct __align__(16) SharedCtl {
     uint64_t q_full, q_empty;
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-    uint64_t drain;
+    uint64_t drain[2];
+    unsigned long long progress[2];  // per tile: (unit sequence << 32) | (last issued key step + 1)
     uint32_t tmem_base;
     int abort;
 };
@@ -221,48 +224,82 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
     }
 }
 
-// --------------------------------------------------------------- MMA issuer
+// -------------------------------------------------------------- MMA issuers
+// One issuing thread per Q tile t: S_t(j) = Q_t K_j^T and O_t += P_t(j) V_j.
+// Each thread keeps its own tile's order (S_t(j+1) after P.V_t(j), since P
+// aliases S); the two threads run independently, so one tile's slow softmax
+// never delays the other tile's MMAs.  A K/V ring slot and the Q buffer are
+// released once both threads have arrived (count 2); a tile with no work on
+// key tile j still waits for that slot to be full before arriving, which
+// keeps the phases of the ring aligned.
 template <int D, bool kBf16>
 __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
-                                         uint32_t sKVa, uint32_t tmem) {
+                                         uint32_t sKVa, uint32_t tmem, int t) {
     using C = TcCfg<D>;
     constexpr uint32_t idesc_s = make_idesc(kBf16, kTileM, kTileN, false);
     constexpr uint32_t idesc_o = make_idesc(kBf16, kTileM, D, true);
-    uint32_t kv_it = 0, q_it = 0;
-    // Per-tile counters as plain scalars: a runtime index into a small array
-    // would push it to local memory.
-    uint32_t p_cnt0 = 0, p_cnt1 = 0, o_cnt0 = 0, o_cnt1 = 0;
+    const uint32_t dS = tmem + (t ? C::kColS1 : C::kColS0);
+    const uint32_t dO = tmem + (t ? C::kColO1 : C::kColO0);
+    const uint32_t qa = sQa + t * C::kTileBytes;
+    const uint32_t s_full = smem_u32(&sh->s_full[t]);
+    const uint32_t p_full = smem_u32(&sh->p_full[t]);
+    const uint32_t o_done = smem_u32(&sh->o_done[t]);
+    const uint32_t o_free = smem_u32(&sh->o_free[t]);
+    const uint32_t q_full = smem_u32(&sh->q_full);
+    const uint32_t q_empty = smem_u32(&sh->q_empty);
+    uint32_t kv_it = 0, q_it = 0, p_cnt = 0, o_cnt = 0;
     bool ok = true;
+    volatile unsigned long long* my_progress = &sh->progress[t];
+    volatile unsigned long long* other_progress = &sh->progress[1 - t];
+    // The two issuers alternate on the tensor core: tile 1 issues key step j
+    // only after tile 0 has, and tile 0 issues step j only after tile 1 has
+    // issued step j - 1.  Each thread still wakes on its own P, so neither
+    // tile's P waits behind the other tile's MMA issue, and the two softmaxes
+    // stay half a step apart instead of competing for the same cycles.
+    auto publish = [&](unsigned long long v) { *my_progress = v; };
+    auto wait_turn = [&](unsigned long long target) {
+        if (*other_progress >= target) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            __nanosleep(20);
+            if (*other_progress >= target) return true;
+            if ((it & 15u) == 0) {
+                if (*W.abort) return false;
+                if (globaltimer_ns() - t0 > W.limit) {
+                    *W.abort = 1;
+                    atomicExch(W.status, DEV_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    };
 
-    // S_t = Q_t K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
-    auto issue_s = [&](int t, int slot) {
-        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+    // S = Q K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
+    auto issue_s = [&](uint32_t slot) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            const uint64_t a = make_sdesc(sQa + t * C::kTileBytes + off, 16, 1024);
+            const uint64_t a = make_sdesc(qa + off, 16, 1024);
             const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + off, 16, 1024);
-            mma_ss(d, a, b, idesc_s, kk > 0);
+            mma_ss(dS, a, b, idesc_s, kk > 0);
         }
-        mma_commit(smem_u32(&sh->s_full[t]));
+        mma_commit(s_full);
     };
-    // O_t += P_t V: P from TMEM (8 columns = 16 keys per step), V MN-major in
+    // O += P V: P from TMEM (8 columns = 16 keys per step), V MN-major in
     // shared memory (16 keys = two 8-row swizzle atoms = 2048 bytes per step;
-    // the second 64-column chunk of V sits one box further on).
-    // With a split P the low halves (64 columns further on) add a second product.
-    auto issue_pv = [&](int t, int slot, bool first, bool split) {
-        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+    // the second 64-column chunk of V sits one box further on).  With a split
+    // P the low halves (64 columns further on) add a second product.
+    auto issue_pv = [&](uint32_t slot, bool first, bool split) {
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
             const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
-            mma_ts(d, a + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+            mma_ts(dO, dS + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
         }
         if (split) {
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk) {
                 const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
-                mma_ts(d, a + 64 + kk * 8, b, idesc_o, 1u);
+                mma_ts(dO, dS + 64 + kk * 8, b, idesc_o, 1u);
             }
         }
     };
@@ -271,72 +308,66 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         tc_fence_after();
         return r;
     };
+    // Give back a slot this tile does not read.
+    auto skip_kv = [&](uint32_t idx) {
+        if (!wait_kv(idx)) return false;
+        mbar_arrive(smem_u32(&sh->kv_empty[idx % C::kStages]));
+        return true;
+    };
 
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
-        if (!(ok = W.wait(smem_u32(&sh->q_full), q_it & 1))) break;
+        if (!(ok = W.wait(q_full, q_it & 1))) break;
         ++q_it;
         tc_fence_after();
         const uint32_t kbase = kv_it;  // ring index of K_jlo; V_j follows K_j
         kv_it += 2 * (un.jhi - un.jlo);
-        const int lo0 = un.lo[0], hi0 = un.hi[0], lo1 = un.lo[1], hi1 = un.hi[1];
-        const bool split0 = kBf16 && tile_split_p(p.g, un.q0);
-        const bool split1 = kBf16 && tile_split_p(p.g, un.q0 + kTileM);
-
-        // One Q tile's share of key step j: P.V for j, then S for j + 1.
-        auto tile_step = [&](auto tc, int j, uint32_t vidx, uint32_t kidx, bool has_next, bool& k_ready) -> bool {
-            constexpr int t = decltype(tc)::value;
-            const int lo = t ? lo1 : lo0;
-            const int hi = t ? hi1 : hi0;
-            uint32_t& pc = t ? p_cnt1 : p_cnt0;
-            uint32_t& oc = t ? o_cnt1 : o_cnt0;
-            if (j >= lo && j < hi) {
-                if (!W.wait(smem_u32(&sh->p_full[t]), pc & 1)) return false;
-                ++pc;
-                const bool first = j == lo;
-                if (first && oc > 0 && !W.wait(smem_u32(&sh->o_free[t]), (oc - 1) & 1)) return false;
-                tc_fence_after();
-                issue_pv(t, vidx % C::kStages, first, t ? split1 : split0);
-                if (j == hi - 1) {
-                    mma_commit(smem_u32(&sh->o_done[t]));
-                    ++oc;
-                }
-            }
-            if (has_next && j + 1 >= lo && j + 1 < hi) {
-                if (!k_ready) {
-                    if (!wait_kv(kidx)) return false;
-                    k_ready = true;
-                }
-                issue_s(t, kidx % C::kStages);
-            }
-            return true;
-        };
-
-        if (!(ok = wait_kv(kbase))) break;
-        if (un.jlo >= lo0 && un.jlo < hi0) issue_s(0, kbase % C::kStages);
-        if (un.jlo >= lo1 && un.jlo < hi1) issue_s(1, kbase % C::kStages);
-        mma_commit(smem_u32(&sh->kv_empty[kbase % C::kStages]));
-
-        for (int j = un.jlo; j < un.jhi && ok; ++j) {
-            const uint32_t vidx = kbase + 2 * (j - un.jlo) + 1;
-            const uint32_t kidx = vidx + 1;
-            const bool has_next = j + 1 < un.jhi;
-            if (!has_next) mma_commit(smem_u32(&sh->q_empty));  // every S of this unit is issued
-            if (!(ok = wait_kv(vidx))) break;
-            bool k_ready = false;
-            ok = tile_step(std::integral_constant<int, 0>{}, j, vidx, kidx, has_next, k_ready) &&
-                 tile_step(std::integral_constant<int, 1>{}, j, vidx, kidx, has_next, k_ready);
-            if (!ok) break;
-            mma_commit(smem_u32(&sh->kv_empty[vidx % C::kStages]));
-            if (has_next) {
-                if (!k_ready && !(ok = wait_kv(kidx))) break;
-                mma_commit(smem_u32(&sh->kv_empty[kidx % C::kStages]));
-            }
+        const int lo = t ? un.lo[1] : un.lo[0];
+        const int hi = t ? un.hi[1] : un.hi[0];
+        const unsigned long long useq = (unsigned long long)q_it << 32;  // q_it counts units taken
+        const int hi0 = un.hi[0], lo0 = un.lo[0], hi1 = un.hi[1], lo1 = un.lo[1];
+        auto kidx = [&](int j) { return kbase + 2 * (uint32_t)(j - un.jlo); };
+        if (lo == hi) {
+            publish(useq | 0xFFFFFFFFull);
+            mbar_arrive(q_empty);
+            for (int j = un.jlo; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
+            continue;
         }
+        const bool split = kBf16 && tile_split_p(p.g, un.q0 + t * kTileM);
+        for (int j = un.jlo; j < lo && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
+        if (!ok || !(ok = wait_kv(kidx(lo)))) break;
+        issue_s(kidx(lo) % C::kStages);
+        mma_commit(smem_u32(&sh->kv_empty[kidx(lo) % C::kStages]));
+        for (int j = lo; j < hi && ok; ++j) {
+            const uint32_t v = kidx(j) + 1;
+            if (j == hi - 1) mma_commit(q_empty);  // this tile's last S is issued
+            if (!(ok = wait_kv(v))) break;
+            if (!(ok = W.wait(p_full, p_cnt & 1))) break;
+            ++p_cnt;
+            const bool first = j == lo;
+            if (first && o_cnt > 0 && !(ok = W.wait(o_free, (o_cnt - 1) & 1))) break;
+            if (t == 1 && lo0 < hi0 && !(ok = wait_turn(useq | (unsigned long long)(j + 1 < hi0 ? j + 1 : hi0)))) break;
+            if (t == 0 && j - 1 >= lo1 && j - 1 < hi1 && !(ok = wait_turn(useq | (unsigned long long)j))) break;
+            tc_fence_after();
+            issue_pv(v % C::kStages, first, split);
+            mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
+            if (j == hi - 1) {
+                mma_commit(o_done);
+                ++o_cnt;
+            } else {
+                const uint32_t k = kidx(j + 1);
+                if (!(ok = wait_kv(k))) break;
+                issue_s(k % C::kStages);
+                mma_commit(smem_u32(&sh->kv_empty[k % C::kStages]));
+            }
+            publish(useq | (unsigned long long)(j + 1));
+        }
+        for (int j = hi; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
     }
     // Every issued MMA must complete before TMEM is released.
-    mma_commit(smem_u32(&sh->drain));
-    W.drain(smem_u32(&sh->drain), 0);
+    const uint32_t drain = smem_u32(&sh->drain[t]);
+    mma_commit(drain);
+    W.drain(drain, 0);
 }
 
 // ------------------------------------------------------ softmax + epilogue
@@ -540,10 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&sh->q_full), 1);
-        mbar_init(smem_u32(&sh->q_empty), 1);
+        mbar_init(smem_u32(&sh->q_empty), 2);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&sh->kv_full[s]), 1);
-            mbar_init(smem_u32(&sh->kv_empty[s]), 1);
+            mbar_init(smem_u32(&sh->kv_empty[s]), 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(smem_u32(&sh->s_full[t]), 1);
@@ -551,7 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
             mbar_init(smem_u32(&sh->o_done[t]), 1);
             mbar_init(smem_u32(&sh->o_free[t]), 128);
         }
-        mbar_init(smem_u32(&sh->drain), 1);
+        sh->progress[0] = 0ull;
+        sh->progress[1] = 0ull;
+        mbar_init(smem_u32(&sh->drain[0]), 1);
+        mbar_init(smem_u32(&sh->drain[1]), 1);
         sh->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -574,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
 
     if (warp < 8) {
         softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, warp, lane);
-    } else if (warp == kWarpMma) {
-        if (lane == 0) mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem);
+    } else if (warp == kWarpMma || warp == kWarpMma1) {
+        if (lane == 0) mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
     } else if (warp == kWarpTma) {
         if (lane == 0) tma_role<D>(p, W, sh, sQa, sKVa);
     }

@@ -39,17 +39,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// One non-blocking-ish probe of the barrier phase (the hardware may suspend
-// the thread for a short, system-defined time).  True once the phase with
-// the given parity has completed.
+// Longest time one probe may keep the thread suspended; the thread wakes as
+// soon as the phase completes, so waiting warps do not take issue slots.
+constexpr uint32_t kSuspendHintNs = 200000;
+
+// One probe of the barrier phase (the thread may sleep up to the hint while
+// the phase is incomplete).  True once the phase with the given parity has
+// completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
