@@ -35,6 +35,8 @@ SIGNATURES = {
     "fa_fwd_bf16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
+    "fa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P]),
     "fa_device_status": (_I, [_P]),
     "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
@@ -102,6 +104,20 @@ def fa_fwd_f32(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, stre
 
 def fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, stream):
     return load().fa_fwd_ex(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, stream)
+
+
+def fa_decode_plan(B, H, Nq, Nk, D, n_splits=0):
+    """(n_splits, workspace_bytes) the decode of this shape uses on the current device."""
+    ns = ctypes.c_int(0)
+    wb = ctypes.c_ulonglong(0)
+    _check(load().fa_decode_plan(B, H, Nq, Nk, D, n_splits, ctypes.byref(ns), ctypes.byref(wb)), "fa_decode_plan")
+    return ns.value, wb.value
+
+
+def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits, workspace,
+              workspace_bytes, stream):
+    return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits,
+                            workspace, workspace_bytes, stream)
 
 
 def fa_device_status(stream=None):
@@ -174,6 +190,41 @@ def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, 
         rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od], s)
     _check(rc, "fa_fwd_ex")
+    return out, lse
+
+
+def attention_decode(q, k, v, scale=None, causal=False, window=None, n_splits=0, out=None, lse=None,
+                     workspace=None, stream=None):
+    """Decode: q [B, H, Nq, D] (Nq <= 16) against a K/V cache [B, H, Nk, D].
+
+    Query i sits at cache position Nk - Nq + i.  The split-K workspace is
+    allocated with torch unless ``workspace`` (a CUDA uint8 tensor of at least
+    the planned size) is given.  Returns (O, LSE)."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nk, D]")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
+        raise ValueError("q, k, v must share one dtype among float16, bfloat16, float32")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mk, wl, wr = mask_args(causal, window)
+    with torch.cuda.device(q.device):
+        ns, wb = fa_decode_plan(B, H, Nq, Nk, D, n_splits)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        if workspace is None and wb > 0:
+            workspace = torch.empty(wb, dtype=torch.uint8, device=q.device)
+        s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+        rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, D,
+                       float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], ns,
+                       workspace.data_ptr() if workspace is not None else None,
+                       workspace.numel() if workspace is not None else 0, s)
+    _check(rc, "fa_decode")
     return out, lse
 
 

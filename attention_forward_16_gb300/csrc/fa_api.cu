@@ -254,6 +254,61 @@ int fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+int fa_decode_plan(int B, int H, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
+                   unsigned long long* workspace_bytes) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return FA_ERR_ARG;
+    DeviceInfo* dev;
+    int rc = device_info(&dev);
+    if (rc != FA_OK) return rc;
+    int ns, chunk;
+    fa::decode_plan((long long)B * H, Nk, dev->sms, n_splits, &ns, &chunk);
+    if (n_splits_out) *n_splits_out = ns;
+    if (workspace_bytes) *workspace_bytes = fa::decode_workspace_bytes((long long)B * H, Nq, D, ns);
+    return FA_OK;
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+              float scale, int mask_kind, int win_l, int win_r, int dtype, int n_splits, void* workspace,
+              unsigned long long workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o) return FA_ERR_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0 || Nq > Nk) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    fa::Geom g;
+    int rc = normalise_mask(mask_kind, win_l, win_r, Nk, &g);
+    if (rc != FA_OK) return rc;
+    if ((long long)B * H > 0x7fffffffLL) return FA_ERR_ARG;
+    if (dtype < FA_F16 || dtype > FA_F32 || (D != 64 && D != 128) || Nq > fa::kDecodeMaxQ) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
+    if (lse && !aligned(lse, 4)) return FA_ERR_ALIGN;
+    DeviceInfo* dev;
+    if ((rc = device_info(&dev)) != FA_OK) return rc;
+    fa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.BH = (long long)B * H;
+    fa::decode_plan(p.BH, Nk, dev->sms, n_splits, &p.n_splits, &p.chunk);
+    const unsigned long long need = fa::decode_workspace_bytes(p.BH, Nq, D, p.n_splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FA_ERR_ARG;
+        if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+        p.part_o = static_cast<float*>(workspace);
+        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              ((unsigned long long)p.BH * p.n_splits * Nq * D * 4 + 255) / 256 * 256);
+    }
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.D = D;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.win_l = g.win_l;
+    p.win_r = g.win_r;
+    cudaError_t e = fa::launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int* out, int cap) {
     if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_ARG;
     fa::Geom g;

@@ -1,0 +1,306 @@
+// Split-K attention decode: a few new queries against a long K/V cache.
+//
+// "FlashAttention extreme optimisation on Ascend NPUs", optimisation four
+// (KV-cache incremental decode) computes one new token's attention over the
+// cached keys, but merges block results with a running average that is not
+// softmax-correct.  Here each CTA takes one split of the cache and produces a
+// normalised partial O_s with its log-sum-exp LSE_s; a combine pass then
+// forms the exact result
+//
+//     LSE = ln sum_s e^{LSE_s},    O = sum_s e^{LSE_s - LSE} O_s
+//
+// (the same identity as the online softmax of "Ascend C advanced practice:
+// high-performance FlashAttention-2-style tile-level fused attention",
+// section 1.2, applied to whole blocks of keys).
+//
+// Decode reads every cached key and value once and does about one FLOP per
+// byte, so it is bound by HBM bandwidth, not by the tensor cores: the kernel
+// streams K and V with coalesced 8- or 16-byte loads (each lane owns D/32
+// consecutive elements of a row; a warp reads whole rows), keeps four keys in
+// flight per warp, and runs the online softmax in fp32 registers.  Query i
+// sits at key position Nk - Nq + i (the new tokens are the last Nq entries of
+// the cache), which sets the causal and window masks.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = 32 * kDecWarps;
+constexpr int kKeysPerIter = 4;
+constexpr float kDecLn2 = 0.69314718055994530942f;
+
+template <typename T, int DV>
+struct Vec;
+template <>
+struct Vec<__half, 2> {
+    using raw = uint32_t;
+    static __device__ __forceinline__ void cvt(raw r, float* f) {
+        const float2 a = __half22float2(*reinterpret_cast<__half2*>(&r));
+        f[0] = a.x; f[1] = a.y;
+    }
+};
+template <>
+struct Vec<__half, 4> {
+    using raw = uint2;
+    static __device__ __forceinline__ void cvt(raw r, float* f) {
+        const float2 a = __half22float2(*reinterpret_cast<__half2*>(&r.x));
+        const float2 b = __half22float2(*reinterpret_cast<__half2*>(&r.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+};
+template <>
+struct Vec<__nv_bfloat16, 2> {
+    using raw = uint32_t;
+    static __device__ __forceinline__ void cvt(raw r, float* f) {
+        f[0] = __uint_as_float(r << 16); f[1] = __uint_as_float(r & 0xFFFF0000u);
+    }
+};
+template <>
+struct Vec<__nv_bfloat16, 4> {
+    using raw = uint2;
+    static __device__ __forceinline__ void cvt(raw r, float* f) {
+        f[0] = __uint_as_float(r.x << 16); f[1] = __uint_as_float(r.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(r.y << 16); f[3] = __uint_as_float(r.y & 0xFFFF0000u);
+    }
+};
+template <>
+struct Vec<float, 2> {
+    using raw = float2;
+    static __device__ __forceinline__ void cvt(raw r, float* f) { f[0] = r.x; f[1] = r.y; }
+};
+template <>
+struct Vec<float, 4> {
+    using raw = float4;
+    static __device__ __forceinline__ void cvt(raw r, float* f) { f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w; }
+};
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ float from_float<float>(float x) { return x; }
+
+__device__ __forceinline__ bool dec_visible(const DecodeParams& p, int i, int j) {
+    const long long pos = (long long)p.Nk - p.Nq + i;
+    if (p.win_l >= 0 && j < pos - p.win_l) return false;
+    if (p.win_r >= 0 && j > pos + p.win_r) return false;
+    return true;
+}
+
+// One CTA = one (b, h, split).  Warps take keys round-robin in groups of four.
+template <typename T, int DV, int NQ>
+__global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecodeParams p) {
+    using V = Vec<T, DV>;
+    constexpr int D = 32 * DV;
+    extern __shared__ float dsm[];  // [warps][NQ][D + 2]: m, l, acc
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = blockIdx.x % p.n_splits;
+    const long long bh = blockIdx.x / p.n_splits;
+    const int k0 = split * p.chunk;
+    const int k1 = min(p.Nk, k0 + p.chunk);
+    const T* qb = static_cast<const T*>(p.q) + (size_t)bh * p.Nq * D;
+    const T* kb = static_cast<const T*>(p.k) + (size_t)bh * p.Nk * D;
+    const T* vb = static_cast<const T*>(p.v) + (size_t)bh * p.Nk * D;
+
+    float q[NQ][DV], acc[NQ][DV], m[NQ], l[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DV; ++e) acc[i][e] = 0.f;
+        if (i < p.Nq) {
+            V::cvt(*reinterpret_cast<const typename V::raw*>(qb + (size_t)i * D + lane * DV), q[i]);
+#pragma unroll
+            for (int e = 0; e < DV; ++e) q[i][e] *= p.scale_log2;  // scores in log2 units
+        } else {
+#pragma unroll
+            for (int e = 0; e < DV; ++e) q[i][e] = 0.f;
+        }
+    }
+
+    for (int base = k0 + warp * kKeysPerIter; base < k1; base += kDecWarps * kKeysPerIter) {
+        typename V::raw kr[kKeysPerIter], vr[kKeysPerIter];
+#pragma unroll
+        for (int u = 0; u < kKeysPerIter; ++u) {
+            const int j = base + u < k1 ? base + u : k1 - 1;  // clamp: tail keys are masked below
+            kr[u] = *reinterpret_cast<const typename V::raw*>(kb + (size_t)j * D + lane * DV);
+            vr[u] = *reinterpret_cast<const typename V::raw*>(vb + (size_t)j * D + lane * DV);
+        }
+        float kf[kKeysPerIter][DV], vf[kKeysPerIter][DV];
+#pragma unroll
+        for (int u = 0; u < kKeysPerIter; ++u) {
+            V::cvt(kr[u], kf[u]);
+            V::cvt(vr[u], vf[u]);
+        }
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            if (i >= p.Nq) break;
+            float s[kKeysPerIter];
+#pragma unroll
+            for (int u = 0; u < kKeysPerIter; ++u) {
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < DV; ++e) d = fmaf(q[i][e], kf[u][e], d);
+                s[u] = d;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int u = 0; u < kKeysPerIter; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kKeysPerIter; ++u) {
+                if (base + u >= k1 || !dec_visible(p, i, base + u)) s[u] = -INFINITY;
+                mx = fmaxf(mx, s[u]);
+            }
+            if (mx == -INFINITY) continue;  // warp-uniform: no visible key in this group
+            if (mx > m[i]) {
+                const float a = m[i] == -INFINITY ? 0.f : ptx::ex2(m[i] - mx);
+                l[i] *= a;
+#pragma unroll
+                for (int e = 0; e < DV; ++e) acc[i][e] *= a;
+                m[i] = mx;
+            }
+#pragma unroll
+            for (int u = 0; u < kKeysPerIter; ++u) {
+                const float pu = ptx::ex2(s[u] - m[i]);
+                l[i] += pu;
+#pragma unroll
+                for (int e = 0; e < DV; ++e) acc[i][e] = fmaf(pu, vf[u][e], acc[i][e]);
+            }
+        }
+    }
+
+    // Merge the four warps' states through shared memory.
+    float* mine = dsm + (size_t)warp * NQ * (D + 2);
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        if (i >= p.Nq) break;
+        if (lane == 0) {
+            mine[i * (D + 2) + D] = m[i];
+            mine[i * (D + 2) + D + 1] = l[i];
+        }
+#pragma unroll
+        for (int e = 0; e < DV; ++e) mine[i * (D + 2) + lane * DV + e] = acc[i][e];
+    }
+    __syncthreads();
+    for (int i = warp; i < p.Nq; i += kDecWarps) {
+        float M = -INFINITY;
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, dsm[((size_t)w * NQ + i) * (D + 2) + D]);
+        float L = 0.f, o[DV];
+#pragma unroll
+        for (int e = 0; e < DV; ++e) o[e] = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kDecWarps; ++w) {
+                const float* st = dsm + ((size_t)w * NQ + i) * (D + 2);
+                const float a = st[D] == -INFINITY ? 0.f : ptx::ex2(st[D] - M);
+                L += a * st[D + 1];
+#pragma unroll
+                for (int e = 0; e < DV; ++e) o[e] = fmaf(a, st[lane * DV + e], o[e]);
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float lse = L > 0.f ? (M + log2f(L)) * kDecLn2 : -INFINITY;
+        const size_t row = (size_t)bh * p.Nq + i;
+        if (p.n_splits == 1) {
+            T* ob = static_cast<T*>(p.o) + row * D + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(o[e] * inv);
+            if (p.lse && lane == 0) p.lse[row] = lse;
+        } else {
+            const size_t prow = ((size_t)bh * p.n_splits + split) * p.Nq + i;
+            float* po = p.part_o + prow * D + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) po[e] = o[e] * inv;
+            if (lane == 0) p.part_lse[prow] = lse;
+        }
+    }
+}
+
+// One warp per output row: O = sum_s e^{LSE_s - LSE} O_s.
+template <typename T, int DV>
+__global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
+    constexpr int D = 32 * DV;
+    const int lane = threadIdx.x & 31;
+    const long long rowid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const long long rows = (long long)p.BH * p.Nq;
+    if (rowid >= rows) return;
+    const long long bh = rowid / p.Nq;
+    const int i = (int)(rowid % p.Nq);
+    float M = -INFINITY;
+    for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, p.part_lse[((size_t)bh * p.n_splits + s) * p.Nq + i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float o[DV];
+#pragma unroll
+    for (int e = 0; e < DV; ++e) o[e] = 0.f;
+    float L = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < p.n_splits; ++s) {
+            const size_t prow = ((size_t)bh * p.n_splits + s) * p.Nq + i;
+            const float ls = p.part_lse[prow];
+            if (ls == -INFINITY) continue;
+            const float w = expf(ls - M);
+            L += w;
+            const float* po = p.part_o + prow * D + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) o[e] = fmaf(w, po[e], o[e]);
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    T* ob = static_cast<T*>(p.o) + (size_t)rowid * D + lane * DV;
+#pragma unroll
+    for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(o[e] * inv);
+    if (p.lse && lane == 0) p.lse[rowid] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+template <typename T, int DV, int NQ>
+cudaError_t launch_split(const DecodeParams& p, cudaStream_t s) {
+    constexpr int D = 32 * DV;
+    const long long blocks = (long long)p.BH * p.n_splits;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(float) * kDecWarps * NQ * (D + 2);
+    auto kern = fa_decode_split_kernel<T, DV, NQ>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)blocks, kDecThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Query count buckets keep the per-row register arrays no larger than needed.
+template <typename T, int DV>
+cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
+    cudaError_t e = p.Nq == 1   ? launch_split<T, DV, 1>(p, s)
+                    : p.Nq <= 4 ? launch_split<T, DV, 4>(p, s)
+                                : launch_split<T, DV, kDecodeMaxQ>(p, s);
+    if (e != cudaSuccess || p.n_splits == 1) return e;
+    const long long rows = (long long)p.BH * p.Nq;
+    fa_decode_combine_kernel<T, DV><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s) {
+    const int dv = p.D / 32;
+    switch (dtype_code) {
+        case 0: return dv == 4 ? launch_typed<__half, 4>(p, s) : launch_typed<__half, 2>(p, s);
+        case 1: return dv == 4 ? launch_typed<__nv_bfloat16, 4>(p, s) : launch_typed<__nv_bfloat16, 2>(p, s);
+        default: return dv == 4 ? launch_typed<float, 4>(p, s) : launch_typed<float, 2>(p, s);
+    }
+}
+
+
+}  // namespace fa

@@ -41,7 +41,53 @@ struct SimtParams {
     float scale;
 };
 
+// Split-K decode: a few queries (the last Nq positions) against an Nk-key cache.
+constexpr int kDecodeMaxQ = 16;   // queries per (b, h) the decode kernels accept
+constexpr int kDecodeMinKeysPerSplit = 256;
+
+struct DecodeParams {
+    const void* q;      // [B*H, Nq, D]
+    const void* k;      // [B*H, Nk, D]
+    const void* v;
+    void* o;            // [B*H, Nq, D]
+    float* lse;         // [B*H, Nq] or null
+    float* part_o;      // [B*H, n_splits, Nq, D] fp32 partial outputs (n_splits > 1)
+    float* part_lse;    // [B*H, n_splits, Nq]
+    long long BH;
+    int Nq;
+    int Nk;
+    int D;
+    float scale_log2;
+    int win_l;          // -1 = unbounded; positions: query i sits at key Nk - Nq + i
+    int win_r;
+    int n_splits;
+    int chunk;          // keys per split (multiple of 4)
+};
+
+// Split count and key chunk for a decode problem (n_req <= 0: choose).
+inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk) {
+    long long s = n_req > 0 ? n_req : (4LL * sms + BH - 1) / BH;
+    const long long cap = (Nk + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
+    if (n_req <= 0 && s > cap) s = cap;
+    if (s > Nk) s = Nk;
+    if (s > 1024) s = 1024;
+    if (s < 1) s = 1;
+    long long c = (Nk + s - 1) / s;
+    c = (c + 3) / 4 * 4;
+    *chunk = (int)c;
+    *n_splits = (int)((Nk + c - 1) / c);
+}
+
+// Bytes of fp32 partials a decode with n_splits splits needs (0 for one split).
+inline unsigned long long decode_workspace_bytes(long long BH, int Nq, int D, int n_splits) {
+    if (n_splits <= 1) return 0;
+    const unsigned long long rows = (unsigned long long)BH * n_splits * Nq;
+    const unsigned long long o_bytes = (rows * D * 4 + 255) / 256 * 256;
+    return o_bytes + (rows * 4 + 255) / 256 * 256;
+}
+
 // Launchers (return the CUDA error of the launch, if any).
+cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s);
 cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s);
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_selftest_timeout(int* status, unsigned long long limit_ns, cudaStream_t s);

@@ -59,6 +59,38 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new queries against an Nk-entry K/V cache (query i at position Nk - Nq + i)."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    D: int
+    dtype: str
+    scale: float
+    mask: int
+    win_l: int = -1
+    win_r: int = -1
+    seed: int = 0
+
+
+DECODE_WORKLOADS = {
+    "bf16_decode_32k": DecodeWorkload("bf16_decode_32k", 8, 32, 1, 32768, 128, "bf16", 1.0 / math.sqrt(128),
+                                      MASK_CAUSAL, seed=1101),
+    "f16_decode_4k_q4": DecodeWorkload("f16_decode_4k_q4", 4, 32, 4, 4096, 128, "f16", 1.0 / math.sqrt(128),
+                                       MASK_CAUSAL, seed=1102),
+}
+
+
+def make_decode(w: DecodeWorkload):
+    """Q [B, H, Nq, D] and the K, V cache [B, H, Nk, D] (K and V from their own stream)."""
+    q, _, _ = make_qkv(w.B, w.H, w.Nq, w.D, w.dtype, seed=w.seed, n_k=1)
+    _, k, v = make_qkv(w.B, w.H, 1, w.D, w.dtype, seed=w.seed + 1, n_k=w.Nk)
+    return q, k, v
+
+
 def torch_dtype(name):
     return _TORCH_DTYPES[name]
 

@@ -371,9 +371,78 @@ def run_native(args, w, world, rank, local, pg):
     return 0
 
 
+def run_decode(args, w, world, rank, local, pg):
+    """Decode against a K/V cache: HBM-bound, reported as achieved GB/s of the
+    compulsory traffic (cache read once, Q read, O and LSE written)."""
+    import torch
+    import attention_forward_16_gb300 as fa
+    from attention_forward_16_gb300.build import build
+    from attention_forward_16_gb300.inputs import make_decode
+
+    build()
+    fa.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    q, k, v = make_decode(w)
+    dq, dk, dv = q.to(device), k.to(device), v.to(device)
+    do = torch.empty_like(dq)
+    dl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
+    ns, wb = fa.fa_decode_plan(w.B, w.H, w.Nq, w.Nk, w.D, 0)
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=device)
+    window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.attention_decode(dq, dk, dv, scale=w.scale, causal=w.mask == fa.FA_MASK_CAUSAL, window=window,
+                            out=do, lse=dl, workspace=ws if wb > 0 else None)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local).start() if rank == 0 else None
+    barrier(pg, device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    clk = clocks.stop() if clocks else None
+    ms = reduce_max(pg, t0.elapsed_time(t1), device) / args.steps
+    e = {"f16": 2, "bf16": 2, "f32": 4}[w.dtype]
+    nbytes = w.B * w.H * (2 * w.Nk * w.D * e + 2 * w.Nq * w.D * e + w.Nq * 4)
+    if rank != 0:
+        return 0
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "attention decode HBM GB/s (split-K, K/V cache read once)", "value": gbs * world, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D, "mask": w.mask,
+                   "n_splits": ns, "workspace_bytes": wb,
+                   "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * w.H * w.Nk * w.D * e >> 20)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "peak_source": src},
+        "clocks": clk, "gpu_launches": args.steps * (2 if ns > 1 else 1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
-    from attention_forward_16_gb300.inputs import WORKLOADS
+    from attention_forward_16_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
+    if args.workload in DECODE_WORKLOADS:
+        world, rank, local, pg = dist_setup(args)
+        try:
+            return run_decode(args, DECODE_WORKLOADS[args.workload], world, rank, local, pg)
+        finally:
+            if pg is not None:
+                pg.destroy_process_group()
     w = WORKLOADS[args.workload]
     if args.batch is not None:
         import dataclasses

@@ -112,6 +112,46 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
               void* stream);
 
 /*
+ * Decode against a key/value cache (split-K).
+ *
+ * The KV-cache incremental decode of "FlashAttention extreme optimisation on
+ * Ascend NPUs" (optimisation four): Nq new queries (1 <= Nq <= 16, Nq <= Nk)
+ * attend to an Nk-entry cache; query i sits at key position Nk - Nq + i, so
+ * FA_MASK_CAUSAL lets it see keys 0 .. Nk - Nq + i and FA_MASK_WINDOW applies
+ * the same band rule around that position.  The cache is split into chunks
+ * handled in parallel; each produces a normalised partial output and its
+ * log-sum-exp, merged exactly as LSE = ln sum_s e^{LSE_s},
+ * O = sum_s e^{LSE_s - LSE} O_s (the page's running-average merge is replaced
+ * by this softmax-correct one).
+ *
+ * Two-phase call, as in the ops-transformer walk-through's aclnn
+ * FlashAttention API (workspace size query, then execute):
+ *
+ * fa_decode_plan -- for the current device, the number of splits a decode of
+ *   this shape uses (n_splits <= 0: chosen to give about four CTAs per SM with
+ *   at least 256 keys each; > 0: that many, capped at Nk) and the workspace it
+ *   needs in bytes (0 when one split suffices).  Returns FA_OK or FA_ERR_ARG.
+ *
+ * fa_decode -- q [B, H, Nq, D], k and v [B, H, Nk, D], o [B, H, Nq, D] (element
+ *   type dtype: FA_F16, FA_BF16 or FA_F32; D in {64, 128}), lse [B, H, Nq] fp32
+ *   or NULL.  `workspace` is caller-owned device memory of at least the size
+ *   fa_decode_plan reported for the same n_splits (256-byte aligned; may be
+ *   NULL when that size is 0); it holds fp32 partial results and must not be
+ *   shared with another call in flight.  Errors: FA_ERR_ARG (null pointer,
+ *   Nq > Nk, a size <= 0, non-finite scale, bad mask, workspace missing or too
+ *   small), FA_ERR_UNSUPPORTED (Nq > 16, D not 64/128, bad dtype),
+ *   FA_ERR_ALIGN (q/k/v/o not 16-byte aligned, workspace not 256-byte
+ *   aligned), FA_ERR_CUDA.  Asynchronous on `stream`.
+ */
+int fa_decode_plan(int B, int H, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
+                   unsigned long long* workspace_bytes);
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int Nq, int Nk, int D, float scale,
+              int mask_kind, int win_l, int win_r, int dtype,
+              int n_splits, void* workspace, unsigned long long workspace_bytes,
+              void* stream);
+
+/*
  * fa_device_status -- synchronise `stream`, then report and clear the
  * library's device status word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel
  * wait ran past its limit; the kernel stopped early and its outputs are

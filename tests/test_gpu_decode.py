@@ -1,0 +1,125 @@
+"""Split-K decode against a K/V cache, checked against the float64 oracle (GPU).
+
+Query i sits at cache position Nk - Nq + i, so the oracle is the plain
+three-pass attention with q_offset = Nk - Nq.  Decode computes in fp32 with
+no 16-bit probabilities, so its error is the output rounding plus fp32
+accumulation: |dO| - half an ulp of O <= 5e-5 for 16-bit outputs,
+|dO| <= 1e-5 for fp32, |dLSE| <= 1e-5.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_16_gb300 as fa
+from attention_forward_16_gb300 import binding as fb
+from attention_forward_16_gb300.inputs import make_qkv
+from oracle import MASK_CAUSAL, MASK_NONE, MASK_WINDOW, attention_three_pass
+
+pytestmark = pytest.mark.gpu
+
+MASKS = [(MASK_NONE, -1, -1), (MASK_CAUSAL, -1, -1), (MASK_WINDOW, 100, 0), (MASK_WINDOW, 5, 2)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_forward_16_gb300.build import build
+    build()
+    fb.load()
+
+
+def _half_ulp(x, dtype):
+    mant = {"f16": 10, "bf16": 7}[dtype]
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    return 0.5 * np.exp2(np.floor(np.log2(ax)) - mant)
+
+
+def _cache(B, H, Nq, Nk, D, dtype, seed):
+    q, _, _ = make_qkv(B, H, Nq, D, dtype, seed=seed, n_k=1)
+    _, k, v = make_qkv(B, H, 1, D, dtype, seed=seed + 1, n_k=Nk)
+    return q, k, v
+
+
+def _decode(q, k, v, scale, mk, wl, wr, n_splits=0):
+    window = (wl, wr) if mk == MASK_WINDOW else None
+    o, lse = fa.attention_decode(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=mk == MASK_CAUSAL,
+                                 window=window, n_splits=n_splits)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def _check(o, lse, q, k, v, scale, mk, wl, wr, dtype, what):
+    Nq, Nk = q.shape[2], k.shape[2]
+    ro, rlse = attention_three_pass(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale, mk, wl, wr,
+                                    q_offset=Nk - Nq)
+    live = np.isfinite(rlse)
+    assert np.array_equal(np.isfinite(lse), live), what
+    err = np.abs(o - ro)
+    if dtype == "f32":
+        assert err.max() <= 1e-5, f"{what}: max|dO| {err.max():.3e}"
+    else:
+        beyond = err - _half_ulp(ro, dtype)
+        assert beyond.max() <= 5e-5, f"{what}: max(|dO| - ulp/2) {beyond.max():.3e}"
+    if live.any():
+        assert np.abs(lse[live] - rlse[live]).max() <= 1e-5, f"{what}: max|dLSE| {np.abs(lse[live] - rlse[live]).max():.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 7), (1, 1000), (3, 255), (4, 4097), (16, 600), (16, 16)])
+def test_decode_matches_oracle(dtype, D, Nq, Nk):
+    q, k, v = _cache(2, 3, Nq, Nk, D, dtype, seed=Nq * 100 + Nk)
+    scale = 1.0 / math.sqrt(D)
+    for mk, wl, wr in MASKS:
+        for ns in (0, 1, 5):
+            o, lse = _decode(q, k, v, scale, mk, wl, wr, ns)
+            _check(o, lse, q, k, v, scale, mk, wl, wr, dtype, f"{dtype} D={D} Nq={Nq} Nk={Nk} mask={mk} splits={ns}")
+
+
+def test_decode_long_cache_many_splits():
+    q, k, v = _cache(1, 8, 1, 65536, 128, "bf16", seed=7)
+    for ns in (0, 64, 300):
+        o, lse = _decode(q, k, v, 0.088, MASK_NONE, -1, -1, ns)
+        _check(o, lse, q, k, v, 0.088, MASK_NONE, -1, -1, "bf16", f"65536 keys, {ns} splits")
+
+
+def test_decode_split_count_does_not_change_result():
+    q, k, v = _cache(2, 4, 2, 3000, 128, "f32", seed=8)
+    base, lbase = _decode(q, k, v, 0.1, MASK_CAUSAL, -1, -1, 1)
+    for ns in (2, 3, 16, 100):
+        o, lse = _decode(q, k, v, 0.1, MASK_CAUSAL, -1, -1, ns)
+        assert np.abs(o - base).max() <= 2e-6 and np.abs(lse - lbase).max() <= 2e-6, ns
+
+
+def test_decode_equals_full_attention_rows():
+    """The last Nq rows of the fused forward on the whole sequence are a decode."""
+    B, H, N, D = 1, 4, 700, 128
+    q, k, v = make_qkv(B, H, N, D, "f16", seed=9)
+    ofull, lfull = fa.attention_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, o_dtype=torch.float32)
+    od, ld = fa.attention_decode(q[:, :, -5:].contiguous().cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    # the fused forward rounds P to fp16 (relative 2^-11); decode keeps P in fp32
+    assert (od.float() - ofull[:, :, -5:]).abs().max().item() <= 2e-3
+    assert (ld - lfull[:, :, -5:]).abs().max().item() <= 1e-3
+
+
+def test_decode_workspace_errors():
+    q, k, v = (t.cuda() for t in _cache(1, 2, 1, 5000, 64, "f16", seed=10))
+    o = torch.empty_like(q)
+    ns, wb = fb.fa_decode_plan(1, 2, 1, 5000, 64, 4)
+    assert ns == 4 and wb > 0
+    ws = torch.empty(wb, dtype=torch.uint8, device="cuda")
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, 1, 2, 1, 5000, 64, 0.1, 0, -1, -1,
+            fb.FA_F16, 4)
+    s = torch.cuda.current_stream().cuda_stream
+    assert fb.fa_decode(*args, None, 0, s) == fb.FA_ERR_ARG
+    assert fb.fa_decode(*args, ws.data_ptr(), wb - 1, s) == fb.FA_ERR_ARG
+    assert fb.fa_decode(*args, ws.data_ptr() + 16, wb, s) == fb.FA_ERR_ALIGN
+    assert fb.fa_decode(*args, ws.data_ptr(), wb, s) == fb.FA_OK
+    torch.cuda.synchronize()
+    ns1, wb1 = fb.fa_decode_plan(1, 2, 1, 5000, 64, 1)
+    assert ns1 == 1 and wb1 == 0

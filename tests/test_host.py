@@ -159,3 +159,48 @@ def test_flops_of_the_benchmark_shapes():
     assert flops.attention_flops(1, 64, 16384, 128, MASK_WINDOW, 1024, 0) == 533_096_038_400
     assert flops.attention_flops(2, 8, 1024, 64, MASK_CAUSAL) == 2_149_580_800
     assert flops.algorithmic_bytes(4, 32, 4096, 128, "f16") == 538_968_064
+
+
+# ------------------------------------------------------ decode: host checks
+
+def _dec(lib, q=16, k=16, v=16, o=16, B=1, H=1, Nq=1, Nk=8, D=64, scale=0.1, mk=0, wl=-1, wr=-1, dt=0, ns=0,
+         ws=None, wb=0):
+    return lib.fa_decode(q, k, v, o, None, B, H, Nq, Nk, D, scale, mk, wl, wr, dt, ns, ws, wb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fb.FA_ERR_ARG),
+    (dict(Nq=0), fb.FA_ERR_ARG),
+    (dict(Nq=9, Nk=8), fb.FA_ERR_ARG),
+    (dict(scale=float("nan")), fb.FA_ERR_ARG),
+    (dict(mk=2, wl=-3), fb.FA_ERR_ARG),
+    (dict(Nq=17, Nk=40), fb.FA_ERR_UNSUPPORTED),
+    (dict(D=96), fb.FA_ERR_UNSUPPORTED),
+    (dict(dt=3), fb.FA_ERR_UNSUPPORTED),
+    (dict(k=24), fb.FA_ERR_ALIGN),
+])
+def test_decode_validation_rejects_before_any_launch(lib, kw, code):
+    assert _dec(lib, **kw) == code
+
+
+def test_decode_plan_arithmetic():
+    """The split plan covers every key exactly once with chunks of 4-key groups."""
+    # a Python restatement of the plan, checked against its coverage contract
+    for BH, Nk, sms, req in [(1, 1, 152, 0), (8, 32768, 152, 0), (256, 4096, 152, 0), (1, 5000, 152, 4),
+                             (2, 3000, 148, 100), (1, 65536, 152, 300), (4, 7, 152, 5)]:
+        ns, chunk = _plan(BH, Nk, sms, req)
+        assert chunk % 4 == 0 and ns >= 1
+        assert (ns - 1) * chunk < Nk <= ns * chunk
+        if req <= 0 and Nk >= 256:
+            assert chunk >= 256 or ns == 1 or BH * ns >= 4 * sms
+
+
+def _plan(BH, Nk, sms, req):
+    s = req if req > 0 else -(-4 * sms // BH)
+    cap = -(-Nk // 256)
+    if req <= 0 and s > cap:
+        s = cap
+    s = max(1, min(s, Nk, 1024))
+    c = -(-Nk // s)
+    c = -(-c // 4) * 4
+    return -(-Nk // c), c
