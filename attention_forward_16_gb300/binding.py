@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libfa.so")
 FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_WINDOW = 0, 1, 2
 FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_OK, FA_ERR_ARG, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+FA_ERR_SCRATCH = -7
 
 _DTYPE_CODE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32}
 
@@ -37,6 +38,8 @@ SIGNATURES = {
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
     "fa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P]),
+    "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
+    "fa_decode_noalloc_scratch_bytes": (ctypes.c_ulonglong, []),
     "fa_device_status": (_I, [_P]),
     "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
@@ -118,6 +121,17 @@ def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, 
               workspace_bytes, stream):
     return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits,
                             workspace, workspace_bytes, stream)
+
+
+def fa_decode_noalloc(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits, stream):
+    """fa_decode with the partial results in the library's fixed scratch array
+    (for callers that must not allocate device memory)."""
+    return load().fa_decode_noalloc(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype,
+                                    n_splits, stream)
+
+
+def fa_decode_noalloc_scratch_bytes():
+    return load().fa_decode_noalloc_scratch_bytes()
 
 
 def fa_device_status(stream=None):

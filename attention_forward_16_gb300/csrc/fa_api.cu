@@ -345,6 +345,7 @@ const char* fa_strerror(int code) {
         case FA_ERR_CUDA: return "CUDA error (see fa_last_cuda_error)";
         case FA_ERR_TIMEOUT: return "a kernel wait timed out";
         case FA_ERR_DEVICE: return "device error reported by the stream";
+        case FA_ERR_SCRATCH: return "partial results exceed the library's fixed scratch array";
         default: return "unknown error code";
     }
 }

@@ -24,7 +24,9 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <mutex>
 
+#include "fa.h"
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -302,5 +304,98 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation.
+//
+// Some callers cannot allocate device memory at the moment they need attention:
+// code running inside an allocator or memory-pool callback, a runtime that has
+// handed all device memory to its own pool and forbids cudaMalloc/cudaFree on
+// the hot path (a cudaMalloc there can block on the device or fail), or a
+// plugin host that gives the library nothing but its input and output buffers.
+// fa_decode_noalloc serves them: the split-K partial results live in a fixed
+// array compiled into this library instead of a caller workspace.
+namespace {
+
+// Room for the fp32 partials (O rows plus their log-sum-exps) of one call.
+constexpr unsigned long long kNoAllocScratchBytes = 16ull << 20;  // 16 MiB on every device that loads the library
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+    std::once_flag once;
+    void* scratch = nullptr;  // device address of g_decode_scratch on this device
+    int sms = 0;
+    cudaError_t err = cudaSuccess;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+bool na_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" int fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                 int Nq, int Nk, int D, float scale, int mask_kind, int win_l, int win_r, int dtype,
+                                 int n_splits, void* stream) {
+    if (!q || !k || !v || !o) return FA_ERR_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0 || Nq > Nk) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    int wl, wr;
+    switch (mask_kind) {
+        case FA_MASK_NONE: wl = -1; wr = -1; break;
+        case FA_MASK_CAUSAL: wl = -1; wr = 0; break;
+        case FA_MASK_WINDOW:
+            if (win_l < -1 || win_r < -1) return FA_ERR_ARG;
+            wl = win_l;
+            wr = win_r;
+            break;
+        default: return FA_ERR_ARG;
+    }
+    if ((long long)B * H > 0x7fffffffLL) return FA_ERR_ARG;
+    if (dtype < FA_F16 || dtype > FA_F32 || (D != 64 && D != 128) || Nq > kDecodeMaxQ) return FA_ERR_UNSUPPORTED;
+    if (!na_aligned(q, 16) || !na_aligned(k, 16) || !na_aligned(v, 16) || !na_aligned(o, 16)) return FA_ERR_ALIGN;
+    if (lse && !na_aligned(lse, 4)) return FA_ERR_ALIGN;
+
+    // Set-up, once per device, with that device current: the host-side name of
+    // the array is not a device address, so ask the runtime for the real one.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return FA_ERR_CUDA;
+    NoAllocDevice& nd = g_noalloc_dev[dev];
+    std::call_once(nd.once, [&] {
+        nd.err = cudaGetSymbolAddress(&nd.scratch, g_decode_scratch);
+        if (nd.err == cudaSuccess) nd.err = cudaDeviceGetAttribute(&nd.sms, cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (nd.err != cudaSuccess || !nd.scratch) return FA_ERR_CUDA;
+
+    DecodeParams p;
+    p.BH = (long long)B * H;
+    decode_plan(p.BH, Nk, nd.sms, n_splits, &p.n_splits, &p.chunk);
+    const unsigned long long need = decode_workspace_bytes(p.BH, Nq, D, p.n_splits);
+    if (need > kNoAllocScratchBytes) return FA_ERR_SCRATCH;
+    p.part_o = nullptr;
+    p.part_lse = nullptr;
+    if (need > 0) {
+        // Every partial row is written before it is read, so nothing in the
+        // array needs clearing between calls.
+        p.part_o = static_cast<float*>(nd.scratch);
+        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(nd.scratch) +
+                                              ((unsigned long long)p.BH * p.n_splits * Nq * D * 4 + 255) / 256 * 256);
+    }
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.D = D;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.win_l = wl;
+    p.win_r = wr;
+    const cudaError_t e = launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" unsigned long long fa_decode_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 }  // namespace fa

@@ -63,8 +63,11 @@ enum {
     FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed; see
                                  fa_last_cuda_error()                          */
     FA_ERR_TIMEOUT = -5,      /* (fa_device_status) a kernel wait timed out    */
-    FA_ERR_DEVICE = -6        /* (fa_device_status) the stream reported a CUDA
+    FA_ERR_DEVICE = -6,       /* (fa_device_status) the stream reported a CUDA
                                  error                                         */
+    FA_ERR_SCRATCH = -7       /* (fa_decode_noalloc) the problem's partial
+                                 results do not fit the library's fixed
+                                 scratch array                                 */
 };
 
 /*
@@ -150,6 +153,37 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
               int mask_kind, int win_l, int win_r, int dtype,
               int n_splits, void* workspace, unsigned long long workspace_bytes,
               void* stream);
+
+/*
+ * fa_decode_noalloc -- fa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point.  It exists for code that
+ * must not call cudaMalloc / cudaFree (or any allocating routine) where it
+ * runs: inside an allocator or memory-pool callback, in a runtime that owns all
+ * device memory through its own pool, or in a plugin that is handed only its
+ * input and output buffers.  It computes what fa_decode computes, with the same
+ * arguments minus the workspace: the split-K partial results go to a fixed
+ * 16 MiB array compiled into the library (fa_decode_noalloc_scratch_bytes()),
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Returns FA_ERR_SCRATCH when the partials of this shape and split count would
+ * not fit (fa_decode_plan's workspace size above the array's size; a smaller
+ * n_splits or a call to fa_decode with a workspace is the way out), otherwise
+ * the codes of fa_decode.  It allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the one array, and it keeps the last call's
+ * contents: calls whose kernels can overlap on the GPU (different streams
+ * without ordering between them) race on it and must be serialised by the
+ * caller.  Nothing in it needs clearing: every partial is written before it is
+ * read.
+ */
+int fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int Nq, int Nk, int D, float scale,
+                      int mask_kind, int win_l, int win_r, int dtype, int n_splits,
+                      void* stream);
+unsigned long long fa_decode_noalloc_scratch_bytes(void);
 
 /*
  * fa_device_status -- synchronise `stream`, then report and clear the
