@@ -132,14 +132,27 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
         }
     }
 
-    for (int base = k0 + warp * kKeysPerIter; base < k1; base += kDecWarps * kKeysPerIter) {
-        typename V::raw kr[kKeysPerIter], vr[kKeysPerIter];
+    // Double-buffered in registers: the next group's loads are issued before
+    // this group's arithmetic, so each warp keeps eight rows of K and V in flight.
+    constexpr int kStride = kDecWarps * kKeysPerIter;
+    typename V::raw kn[kKeysPerIter], vn[kKeysPerIter];
+    auto load_group = [&](int base) {
 #pragma unroll
         for (int u = 0; u < kKeysPerIter; ++u) {
             const int j = base + u < k1 ? base + u : k1 - 1;  // clamp: tail keys are masked below
-            kr[u] = *reinterpret_cast<const typename V::raw*>(kb + (size_t)j * D + lane * DV);
-            vr[u] = *reinterpret_cast<const typename V::raw*>(vb + (size_t)j * D + lane * DV);
+            kn[u] = *reinterpret_cast<const typename V::raw*>(kb + (size_t)j * D + lane * DV);
+            vn[u] = *reinterpret_cast<const typename V::raw*>(vb + (size_t)j * D + lane * DV);
         }
+    };
+    if (k0 + warp * kKeysPerIter < k1) load_group(k0 + warp * kKeysPerIter);
+    for (int base = k0 + warp * kKeysPerIter; base < k1; base += kStride) {
+        typename V::raw kr[kKeysPerIter], vr[kKeysPerIter];
+#pragma unroll
+        for (int u = 0; u < kKeysPerIter; ++u) {
+            kr[u] = kn[u];
+            vr[u] = vn[u];
+        }
+        if (base + kStride < k1) load_group(base + kStride);
         float kf[kKeysPerIter][DV], vf[kKeysPerIter][DV];
 #pragma unroll
         for (int u = 0; u < kKeysPerIter; ++u) {

@@ -66,7 +66,7 @@ struct DecodeParams {
 
 // Split count and key chunk for a decode problem (n_req <= 0: choose).
 inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk) {
-    long long s = n_req > 0 ? n_req : (4LL * sms + BH - 1) / BH;
+    long long s = n_req > 0 ? n_req : (8LL * sms + BH - 1) / BH;
     const long long cap = (Nk + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
     if (n_req <= 0 && s > cap) s = cap;
     if (s > Nk) s = Nk;

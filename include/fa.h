@@ -131,7 +131,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * FlashAttention API (workspace size query, then execute):
  *
  * fa_decode_plan -- for the current device, the number of splits a decode of
- *   this shape uses (n_splits <= 0: chosen to give about four CTAs per SM with
+ *   this shape uses (n_splits <= 0: chosen to give about eight CTAs per SM with
  *   at least 256 keys each; > 0: that many, capped at Nk) and the workspace it
  *   needs in bytes (0 when one split suffices).  Returns FA_OK or FA_ERR_ARG.
  *

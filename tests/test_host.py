@@ -192,11 +192,11 @@ def test_decode_plan_arithmetic():
         assert chunk % 4 == 0 and ns >= 1
         assert (ns - 1) * chunk < Nk <= ns * chunk
         if req <= 0 and Nk >= 256:
-            assert chunk >= 256 or ns == 1 or BH * ns >= 4 * sms
+            assert chunk >= 256 or ns == 1 or BH * ns >= 8 * sms
 
 
 def _plan(BH, Nk, sms, req):
-    s = req if req > 0 else -(-4 * sms // BH)
+    s = req if req > 0 else -(-8 * sms // BH)
     cap = -(-Nk // 256)
     if req <= 0 and s > cap:
         s = cap
