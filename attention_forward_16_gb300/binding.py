@@ -19,6 +19,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfa.so")
 
 FA_MASK_NONE, FA_MASK_CAUSAL, FA_MASK_WINDOW = 0, 1, 2
+FA_LAYOUT_BHND, FA_LAYOUT_BNHD = 0, 1
+_LAYOUT_CODE = {"bhnd": FA_LAYOUT_BHND, "bnhd": FA_LAYOUT_BNHD}
 FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_OK, FA_ERR_ARG, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
 FA_ERR_SCRATCH = -7
@@ -36,8 +38,12 @@ SIGNATURES = {
     "fa_fwd_bf16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_fwd_f32": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _P]),
     "fa_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _I, _P]),
     "fa_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P]),
+    "fa_decode_plan_gqa": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _I, _P,
+                           ctypes.c_ulonglong, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
     "fa_decode_noalloc_scratch_bytes": (ctypes.c_ulonglong, []),
     "fa_device_status": (_I, [_P]),
@@ -117,6 +123,20 @@ def fa_decode_plan(B, H, Nq, Nk, D, n_splits=0):
     return ns.value, wb.value
 
 
+def fa_decode_plan_gqa(B, H, H_kv, Nq, Nk, D, n_splits=0):
+    ns = ctypes.c_int(0)
+    wb = ctypes.c_ulonglong(0)
+    _check(load().fa_decode_plan_gqa(B, H, H_kv, Nq, Nk, D, n_splits, ctypes.byref(ns), ctypes.byref(wb)),
+           "fa_decode_plan_gqa")
+    return ns.value, wb.value
+
+
+def fa_decode_gqa(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, layout, n_splits,
+                  workspace, workspace_bytes, stream):
+    return load().fa_decode_gqa(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype,
+                                layout, n_splits, workspace, workspace_bytes, stream)
+
+
 def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits, workspace,
               workspace_bytes, stream):
     return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits,
@@ -132,6 +152,11 @@ def fa_decode_noalloc(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l,
 
 def fa_decode_noalloc_scratch_bytes():
     return load().fa_decode_noalloc_scratch_bytes()
+
+
+def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, layout, stream):
+    return load().fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype,
+                             layout, stream)
 
 
 def fa_device_status(stream=None):
@@ -173,60 +198,86 @@ def mask_args(causal=False, window=None):
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, out=None, lse=None,
-                  stream=None):
-    """O, LSE = softmax(scale * Q K^T + mask) V for [B, H, N, D] CUDA tensors.
+                  stream=None, layout="bhnd"):
+    """O, LSE = softmax(scale * Q K^T + mask) V for CUDA tensors.
 
-    ``window=(left, right)`` selects the sliding window (None or -1 for an
-    unbounded side); ``scale`` defaults to 1/sqrt(D); ``o_dtype=torch.float32``
-    returns O in fp32 for 16-bit inputs.  Runs on the current CUDA stream
-    unless ``stream`` (a torch.cuda.Stream) is given.
+    ``layout="bhnd"``: q [B, H, N, D], k and v [B, H_kv, N, D];
+    ``layout="bnhd"``: q [B, N, H, D], k and v [B, N, H_kv, D].  H must be a
+    multiple of H_kv (grouped-query attention when smaller).  O has q's shape,
+    LSE is [B, H, N].  ``window=(left, right)`` selects the sliding window
+    (None or -1 for an unbounded side); ``scale`` defaults to 1/sqrt(D);
+    ``o_dtype=torch.float32`` returns O in fp32 for 16-bit inputs.  Runs on
+    the current CUDA stream unless ``stream`` (a torch.cuda.Stream) is given.
     """
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError(f"q, k, v must share one [B, H, N, D] shape, got {tuple(q.shape)}, "
+    if layout not in _LAYOUT_CODE:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError(f"q, k, v must be 4-D with k and v alike, got {tuple(q.shape)}, "
                          f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if layout == "bhnd":
+        B, H, N, D = q.shape
+        Hkv = k.shape[1]
+        ok_shape = k.shape[0] == B and k.shape[2] == N and k.shape[3] == D
+    else:
+        B, N, H, D = q.shape
+        Hkv = k.shape[2]
+        ok_shape = k.shape[0] == B and k.shape[1] == N and k.shape[3] == D
+    if not ok_shape or Hkv < 1 or H % Hkv:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)} for layout {layout}")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
         raise ValueError("q, k, v must share one dtype among float16, bfloat16, float32")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
-    B, H, N, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     mk, wl, wr = mask_args(causal, window)
     od = q.dtype if o_dtype is None else o_dtype
     if out is None:
-        out = torch.empty((B, H, N, D), dtype=od, device=q.device)
+        out = torch.empty(q.shape, dtype=od, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
     with torch.cuda.device(q.device):
-        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od], s)
-    _check(rc, "fa_fwd_ex")
+        rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                        B, H, Hkv, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od],
+                        _LAYOUT_CODE[layout], s)
+    _check(rc, "fa_fwd_gqa")
     return out, lse
 
 
 def attention_decode(q, k, v, scale=None, causal=False, window=None, n_splits=0, out=None, lse=None,
-                     workspace=None, stream=None):
-    """Decode: q [B, H, Nq, D] (Nq <= 16) against a K/V cache [B, H, Nk, D].
+                     workspace=None, stream=None, layout="bhnd"):
+    """Decode: queries against a K/V cache.
 
-    Query i sits at cache position Nk - Nq + i.  The split-K workspace is
-    allocated with torch unless ``workspace`` (a CUDA uint8 tensor of at least
-    the planned size) is given.  Returns (O, LSE)."""
-    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
-        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H, Nk, D]")
+    ``layout="bhnd"``: q [B, H, Nq, D], k and v [B, H_kv, Nk, D];
+    ``layout="bnhd"``: q [B, Nq, H, D], k and v [B, Nk, H_kv, D].  H must be a
+    multiple of H_kv and (H / H_kv) * Nq <= 16.  Query i sits at cache
+    position Nk - Nq + i.  The split-K workspace is allocated with torch
+    unless ``workspace`` (a CUDA uint8 tensor of at least the planned size) is
+    given.  Returns (O, LSE), LSE [B, H, Nq]."""
+    if layout not in _LAYOUT_CODE:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q, k, v must be 4-D with k and v alike")
+    if layout == "bhnd":
+        B, H, Nq, D = q.shape
+        Hkv, Nk = k.shape[1], k.shape[2]
+    else:
+        B, Nq, H, D = q.shape
+        Nk, Hkv = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != D or Hkv < 1 or H % Hkv:
+        raise ValueError(f"k/v shape {tuple(k.shape)} does not match q {tuple(q.shape)} for layout {layout}")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
         raise ValueError("q, k, v must share one dtype among float16, bfloat16, float32")
     if not (q.is_cuda and k.is_cuda and v.is_cuda and q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous CUDA tensors")
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     mk, wl, wr = mask_args(causal, window)
     with torch.cuda.device(q.device):
-        ns, wb = fa_decode_plan(B, H, Nq, Nk, D, n_splits)
+        ns, wb = fa_decode_plan_gqa(B, H, Hkv, Nq, Nk, D, n_splits)
         if out is None:
             out = torch.empty_like(q)
         if lse is None:
@@ -234,11 +285,11 @@ def attention_decode(q, k, v, scale=None, causal=False, window=None, n_splits=0,
         if workspace is None and wb > 0:
             workspace = torch.empty(wb, dtype=torch.uint8, device=q.device)
         s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
-        rc = fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, D,
-                       float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], ns,
-                       workspace.data_ptr() if workspace is not None else None,
-                       workspace.numel() if workspace is not None else 0, s)
-    _check(rc, "fa_decode")
+        rc = fa_decode_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq,
+                           Nk, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _LAYOUT_CODE[layout], ns,
+                           workspace.data_ptr() if workspace is not None else None,
+                           workspace.numel() if workspace is not None else 0, s)
+    _check(rc, "fa_decode_gqa")
     return out, lse
 
 

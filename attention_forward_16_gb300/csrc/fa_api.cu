@@ -77,17 +77,27 @@ int encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return FA_OK;
 }
 
-// 3-D view [B*H][N][D] of a 16-bit tensor; box = 128 rows x 64 columns
-// (128 bytes: the widest box the 128-byte swizzle allows).
-int make_map(CUtensorMap* m, const void* base, bool bf16, int BH, int N, int D) {
+// 4-D view of a 16-bit [B, H, N, D] or [B, N, H, D] tensor with the rows (N)
+// as the box's second dimension; box = 128 rows x 64 columns (128 bytes: the
+// widest box the 128-byte swizzle allows).
+int make_map(CUtensorMap* m, const void* base, bool bf16, int layout, int B, int Hx, int N, int D) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = encoder(&enc);
     if (rc != FA_OK) return rc;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)fa::kTileM, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    if (layout == fa::LAYOUT_BHND) {
+        dims[0] = D; dims[1] = N; dims[2] = Hx; dims[3] = B;
+        strides[0] = (cuuint64_t)D * e; strides[1] = (cuuint64_t)N * D * e; strides[2] = (cuuint64_t)Hx * N * D * e;
+        box[0] = 64; box[1] = fa::kTileM; box[2] = 1; box[3] = 1;
+    } else {
+        dims[0] = D; dims[1] = Hx; dims[2] = N; dims[3] = B;
+        strides[0] = (cuuint64_t)D * e; strides[1] = (cuuint64_t)Hx * D * e; strides[2] = (cuuint64_t)N * Hx * D * e;
+        box[0] = 64; box[1] = 1; box[2] = fa::kTileM; box[3] = 1;
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -146,11 +156,14 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
 
 extern "C" {
 
-int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
-              float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, void* stream) {
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+               int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout,
+               void* stream) {
     fa::Geom g;
     int rc = validate(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, &g);
     if (rc != FA_OK) return rc;
+    if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
     DeviceInfo* dev;
     if ((rc = device_info(&dev)) != FA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -167,6 +180,9 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         p.BH = BH;
         p.D = D;
         p.scale = scale;
+        p.H = H;
+        p.G = H / H_kv;
+        p.layout = layout;
         cudaError_t e = fa::launch_simt_f32(p, s);
         return e == cudaSuccess ? FA_OK : cuda_fail(e);
     }
@@ -174,13 +190,16 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const bool bf16 = dtype == FA_BF16;
     fa::TcParams p;
     std::memset(&p, 0, sizeof(p));
-    if ((rc = make_map(&p.tm_q, q, bf16, BH, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_k, k, bf16, BH, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_v, v, bf16, BH, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_q, q, bf16, layout, B, H, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
     p.o = o;
     p.lse = lse;
     p.g = g;
     p.BH = BH;
+    p.H = H;
+    p.G = H / H_kv;
+    p.layout = layout;
     const long long units = (long long)BH * fa::n_pairs_for(N);
     if (units > 0x7fffffffLL) return FA_ERR_ARG;
     p.n_units = (int)units;
@@ -192,6 +211,12 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
     cudaError_t e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+              float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, void* stream) {
+    return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, FA_LAYOUT_BHND,
+                      stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D, float scale,
@@ -254,45 +279,59 @@ int fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
-int fa_decode_plan(int B, int H, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
-                   unsigned long long* workspace_bytes) {
+int fa_decode_plan_gqa(int B, int H, int H_kv, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
+                       unsigned long long* workspace_bytes) {
     if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return FA_ERR_ARG;
+    if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
     DeviceInfo* dev;
     int rc = device_info(&dev);
     if (rc != FA_OK) return rc;
     int ns, chunk;
-    fa::decode_plan((long long)B * H, Nk, dev->sms, n_splits, &ns, &chunk);
+    const long long groups = (long long)B * H_kv;
+    fa::decode_plan(groups, Nk, dev->sms, n_splits, &ns, &chunk);
     if (n_splits_out) *n_splits_out = ns;
-    if (workspace_bytes) *workspace_bytes = fa::decode_workspace_bytes((long long)B * H, Nq, D, ns);
+    if (workspace_bytes) *workspace_bytes = fa::decode_workspace_bytes(groups, (H / H_kv) * Nq, D, ns);
     return FA_OK;
 }
 
-int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
-              float scale, int mask_kind, int win_l, int win_r, int dtype, int n_splits, void* workspace,
-              unsigned long long workspace_bytes, void* stream) {
+int fa_decode_plan(int B, int H, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
+                   unsigned long long* workspace_bytes) {
+    return fa_decode_plan_gqa(B, H, H, Nq, Nk, D, n_splits, n_splits_out, workspace_bytes);
+}
+
+int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+                  int Nk, int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int layout,
+                  int n_splits, void* workspace, unsigned long long workspace_bytes, void* stream) {
     if (!q || !k || !v || !o) return FA_ERR_ARG;
     if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || D <= 0 || Nq > Nk) return FA_ERR_ARG;
+    if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
     if (!std::isfinite(scale)) return FA_ERR_ARG;
     fa::Geom g;
     int rc = normalise_mask(mask_kind, win_l, win_r, Nk, &g);
     if (rc != FA_OK) return rc;
     if ((long long)B * H > 0x7fffffffLL) return FA_ERR_ARG;
-    if (dtype < FA_F16 || dtype > FA_F32 || (D != 64 && D != 128) || Nq > fa::kDecodeMaxQ) return FA_ERR_UNSUPPORTED;
+    const int G = H / H_kv;
+    if (dtype < FA_F16 || dtype > FA_F32 || (D != 64 && D != 128) || (long long)G * Nq > fa::kDecodeMaxQ)
+        return FA_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
     if (lse && !aligned(lse, 4)) return FA_ERR_ALIGN;
     DeviceInfo* dev;
     if ((rc = device_info(&dev)) != FA_OK) return rc;
     fa::DecodeParams p;
     std::memset(&p, 0, sizeof(p));
-    p.BH = (long long)B * H;
+    p.BH = (long long)B * H_kv;
+    p.G = G;
+    p.Hkv = H_kv;
+    p.layout = layout;
     fa::decode_plan(p.BH, Nk, dev->sms, n_splits, &p.n_splits, &p.chunk);
-    const unsigned long long need = fa::decode_workspace_bytes(p.BH, Nq, D, p.n_splits);
+    const unsigned long long need = fa::decode_workspace_bytes(p.BH, G * Nq, D, p.n_splits);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return FA_ERR_ARG;
         if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
         p.part_o = static_cast<float*>(workspace);
         p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                              ((unsigned long long)p.BH * p.n_splits * Nq * D * 4 + 255) / 256 * 256);
+                                              ((unsigned long long)p.BH * p.n_splits * G * Nq * D * 4 + 255) / 256 * 256);
     }
     p.q = q;
     p.k = k;
@@ -307,6 +346,13 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.win_r = g.win_r;
     cudaError_t e = fa::launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+              float scale, int mask_kind, int win_l, int win_r, int dtype, int n_splits, void* workspace,
+              unsigned long long workspace_bytes, void* stream) {
+    return fa_decode_gqa(q, k, v, o, lse, B, H, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, FA_LAYOUT_BHND,
+                         n_splits, workspace, workspace_bytes, stream);
 }
 
 int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int* out, int cap) {

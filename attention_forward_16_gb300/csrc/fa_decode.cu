@@ -92,6 +92,20 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 template <>
 __device__ __forceinline__ float from_float<float>(float x) { return x; }
 
+// Element offsets of query row r (= g * Nq + i: query head g of the group,
+// query i) and of key/value row j, for the (batch, K/V head) group bhk.
+__device__ __forceinline__ size_t dec_qrow(const DecodeParams& p, long long bhk, int r, int D) {
+    const int g = r / p.Nq, i = r % p.Nq;
+    if (p.layout == LAYOUT_BHND) return ((size_t)(bhk * p.G + g) * p.Nq + i) * D;
+    const long long b = bhk / p.Hkv, h = (bhk % p.Hkv) * p.G + g;
+    return (((size_t)b * p.Nq + i) * ((size_t)p.Hkv * p.G) + h) * D;
+}
+__device__ __forceinline__ size_t dec_krow(const DecodeParams& p, long long bhk, int j, int D) {
+    if (p.layout == LAYOUT_BHND) return ((size_t)bhk * p.Nk + j) * D;
+    const long long b = bhk / p.Hkv, hk = bhk % p.Hkv;
+    return (((size_t)b * p.Nk + j) * p.Hkv + hk) * D;
+}
+
 __device__ __forceinline__ bool dec_visible(const DecodeParams& p, int i, int j) {
     const long long pos = (long long)p.Nk - p.Nq + i;
     if (p.win_l >= 0 && j < pos - p.win_l) return false;
@@ -111,9 +125,10 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
     const long long bh = blockIdx.x / p.n_splits;
     const int k0 = split * p.chunk;
     const int k1 = min(p.Nk, k0 + p.chunk);
-    const T* qb = static_cast<const T*>(p.q) + (size_t)bh * p.Nq * D;
-    const T* kb = static_cast<const T*>(p.k) + (size_t)bh * p.Nk * D;
-    const T* vb = static_cast<const T*>(p.v) + (size_t)bh * p.Nk * D;
+    const int rows = p.G * p.Nq;
+    const T* qg = static_cast<const T*>(p.q);
+    const T* kg = static_cast<const T*>(p.k);
+    const T* vg = static_cast<const T*>(p.v);
 
     float q[NQ][DV], acc[NQ][DV], m[NQ], l[NQ];
 #pragma unroll
@@ -122,8 +137,8 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
         l[i] = 0.f;
 #pragma unroll
         for (int e = 0; e < DV; ++e) acc[i][e] = 0.f;
-        if (i < p.Nq) {
-            V::cvt(*reinterpret_cast<const typename V::raw*>(qb + (size_t)i * D + lane * DV), q[i]);
+        if (i < rows) {
+            V::cvt(*reinterpret_cast<const typename V::raw*>(qg + dec_qrow(p, bh, i, D) + lane * DV), q[i]);
 #pragma unroll
             for (int e = 0; e < DV; ++e) q[i][e] *= p.scale_log2;  // scores in log2 units
         } else {
@@ -140,8 +155,9 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
 #pragma unroll
         for (int u = 0; u < kKeysPerIter; ++u) {
             const int j = base + u < k1 ? base + u : k1 - 1;  // clamp: tail keys are masked below
-            kn[u] = *reinterpret_cast<const typename V::raw*>(kb + (size_t)j * D + lane * DV);
-            vn[u] = *reinterpret_cast<const typename V::raw*>(vb + (size_t)j * D + lane * DV);
+            const size_t kr_off = dec_krow(p, bh, j, D) + lane * DV;
+            kn[u] = *reinterpret_cast<const typename V::raw*>(kg + kr_off);
+            vn[u] = *reinterpret_cast<const typename V::raw*>(vg + kr_off);
         }
     };
     if (k0 + warp * kKeysPerIter < k1) load_group(k0 + warp * kKeysPerIter);
@@ -161,7 +177,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
         }
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
-            if (i >= p.Nq) break;
+            if (i >= rows) break;
             float s[kKeysPerIter];
 #pragma unroll
             for (int u = 0; u < kKeysPerIter; ++u) {
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
             float mx = -INFINITY;
 #pragma unroll
             for (int u = 0; u < kKeysPerIter; ++u) {
-                if (base + u >= k1 || !dec_visible(p, i, base + u)) s[u] = -INFINITY;
+                if (base + u >= k1 || !dec_visible(p, i % p.Nq, base + u)) s[u] = -INFINITY;
                 mx = fmaxf(mx, s[u]);
             }
             if (mx == -INFINITY) continue;  // warp-uniform: no visible key in this group
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
     float* mine = dsm + (size_t)warp * NQ * (D + 2);
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
-        if (i >= p.Nq) break;
+        if (i >= rows) break;
         if (lane == 0) {
             mine[i * (D + 2) + D] = m[i];
             mine[i * (D + 2) + D + 1] = l[i];
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
         for (int e = 0; e < DV; ++e) mine[i * (D + 2) + lane * DV + e] = acc[i][e];
     }
     __syncthreads();
-    for (int i = warp; i < p.Nq; i += kDecWarps) {
+    for (int i = warp; i < rows; i += kDecWarps) {
         float M = -INFINITY;
         for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, dsm[((size_t)w * NQ + i) * (D + 2) + D]);
         float L = 0.f, o[DV];
@@ -228,14 +244,13 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const float lse = L > 0.f ? (M + log2f(L)) * kDecLn2 : -INFINITY;
-        const size_t row = (size_t)bh * p.Nq + i;
         if (p.n_splits == 1) {
-            T* ob = static_cast<T*>(p.o) + row * D + lane * DV;
+            T* ob = static_cast<T*>(p.o) + dec_qrow(p, bh, i, D) + lane * DV;
 #pragma unroll
             for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(o[e] * inv);
-            if (p.lse && lane == 0) p.lse[row] = lse;
+            if (p.lse && lane == 0) p.lse[(size_t)bh * rows + i] = lse;   // [B, H, Nq] row of query head g, query i
         } else {
-            const size_t prow = ((size_t)bh * p.n_splits + split) * p.Nq + i;
+            const size_t prow = ((size_t)bh * p.n_splits + split) * rows + i;
             float* po = p.part_o + prow * D + lane * DV;
 #pragma unroll
             for (int e = 0; e < DV; ++e) po[e] = o[e] * inv;
@@ -249,13 +264,13 @@ template <typename T, int DV>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
     constexpr int D = 32 * DV;
     const int lane = threadIdx.x & 31;
+    const int rows = p.G * p.Nq;
     const long long rowid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const long long rows = (long long)p.BH * p.Nq;
-    if (rowid >= rows) return;
-    const long long bh = rowid / p.Nq;
-    const int i = (int)(rowid % p.Nq);
+    if (rowid >= (long long)p.BH * rows) return;
+    const long long bh = rowid / rows;
+    const int i = (int)(rowid % rows);
     float M = -INFINITY;
-    for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, p.part_lse[((size_t)bh * p.n_splits + s) * p.Nq + i]);
+    for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, p.part_lse[((size_t)bh * p.n_splits + s) * rows + i]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float o[DV];
@@ -264,7 +279,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
     float L = 0.f;
     if (M != -INFINITY) {
         for (int s = 0; s < p.n_splits; ++s) {
-            const size_t prow = ((size_t)bh * p.n_splits + s) * p.Nq + i;
+            const size_t prow = ((size_t)bh * p.n_splits + s) * rows + i;
             const float ls = p.part_lse[prow];
             if (ls == -INFINITY) continue;
             const float w = expf(ls - M);
@@ -275,7 +290,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodePara
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    T* ob = static_cast<T*>(p.o) + (size_t)rowid * D + lane * DV;
+    T* ob = static_cast<T*>(p.o) + dec_qrow(p, bh, i, D) + lane * DV;
 #pragma unroll
     for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(o[e] * inv);
     if (p.lse && lane == 0) p.lse[rowid] = L > 0.f ? M + logf(L) : -INFINITY;
@@ -297,12 +312,13 @@ cudaError_t launch_split(const DecodeParams& p, cudaStream_t s) {
 // Query count buckets keep the per-row register arrays no larger than needed.
 template <typename T, int DV>
 cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
-    cudaError_t e = p.Nq == 1   ? launch_split<T, DV, 1>(p, s)
-                    : p.Nq <= 4 ? launch_split<T, DV, 4>(p, s)
+    const int rows = p.G * p.Nq;
+    cudaError_t e = rows == 1   ? launch_split<T, DV, 1>(p, s)
+                    : rows <= 4 ? launch_split<T, DV, 4>(p, s)
                                 : launch_split<T, DV, kDecodeMaxQ>(p, s);
     if (e != cudaSuccess || p.n_splits == 1) return e;
-    const long long rows = (long long)p.BH * p.Nq;
-    fa_decode_combine_kernel<T, DV><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(p);
+    const long long all_rows = (long long)p.BH * rows;
+    fa_decode_combine_kernel<T, DV><<<(unsigned)((all_rows + 3) / 4), 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -13,14 +13,25 @@ namespace fa {
 enum DeviceStatus { DEV_OK = 0, DEV_TIMEOUT = 1 };
 
 // Parameters of the tensor-core kernel (passed as one __grid_constant__).
+// Memory layouts of Q, K, V and O.
+enum Layout { LAYOUT_BHND = 0, LAYOUT_BNHD = 1 };
+
+// Row offset (in elements / D) of query or key row i of head h, batch b.
+FA_HD long long row_index(int layout, int b, int h, int i, int H, int N) {
+    return layout == LAYOUT_BHND ? ((long long)b * H + h) * N + i : ((long long)b * N + i) * H + h;
+}
+
 struct TcParams {
-    CUtensorMap tm_q;   // 3-D maps over [B*H, N, D] 16-bit, box {64, 128, 1}, 128B swizzle
-    CUtensorMap tm_k;
+    CUtensorMap tm_q;   // 4-D maps: {D, N, H, B} ([B,H,N,D]) or {D, H, N, B} ([B,N,H,D]);
+    CUtensorMap tm_k;   // 16-bit, box of 128 rows x 64 columns, 128-byte swizzle
     CUtensorMap tm_v;
-    void* o;            // [B*H, N, D], 16-bit or fp32 (o_f32)
-    float* lse;         // [B*H, N] or null
+    void* o;            // O in Q's layout, 16-bit or fp32 (o_f32)
+    float* lse;         // [B, H, N] or null
     Geom g;
     int BH;
+    int H;              // query heads
+    int G;              // query heads per K/V head (H / H_kv)
+    int layout;
     int n_units;
     int order;
     float scale_log2;   // scale * log2(e)
@@ -39,6 +50,9 @@ struct SimtParams {
     int BH;
     int D;
     float scale;
+    int H = 1;          // query heads
+    int G = 1;          // query heads per K/V head
+    int layout = LAYOUT_BHND;
 };
 
 // Split-K decode: a few queries (the last Nq positions) against an Nk-key cache.
@@ -46,14 +60,14 @@ constexpr int kDecodeMaxQ = 16;   // queries per (b, h) the decode kernels accep
 constexpr int kDecodeMinKeysPerSplit = 256;
 
 struct DecodeParams {
-    const void* q;      // [B*H, Nq, D]
-    const void* k;      // [B*H, Nk, D]
+    const void* q;      // [B, H, Nq, D] or [B, Nq, H, D]
+    const void* k;      // [B, H_kv, Nk, D] or [B, Nk, H_kv, D]
     const void* v;
-    void* o;            // [B*H, Nq, D]
-    float* lse;         // [B*H, Nq] or null
-    float* part_o;      // [B*H, n_splits, Nq, D] fp32 partial outputs (n_splits > 1)
-    float* part_lse;    // [B*H, n_splits, Nq]
-    long long BH;
+    void* o;            // Q's shape and layout
+    float* lse;         // [B, H, Nq] or null
+    float* part_o;      // [B*H_kv, n_splits, G*Nq, D] fp32 partial outputs (n_splits > 1)
+    float* part_lse;    // [B*H_kv, n_splits, G*Nq]
+    long long BH;       // B * H_kv: one CTA group per (batch, K/V head)
     int Nq;
     int Nk;
     int D;
@@ -62,6 +76,9 @@ struct DecodeParams {
     int win_r;
     int n_splits;
     int chunk;          // keys per split (multiple of 4)
+    int G = 1;          // query heads per K/V head; a CTA takes all G * Nq query rows of its K/V head
+    int Hkv = 1;        // K/V heads (read only for [B, N, H, D])
+    int layout = LAYOUT_BHND;
 };
 
 // Split count and key chunk for a decode problem (n_req <= 0: choose).

@@ -45,11 +45,13 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_f32_kernel(const SimtParams p
     const int r0 = (blockIdx.x % n_rb) * kRows;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const size_t head = (size_t)bh * N * D;
+    const int b = bh / p.H, h = bh % p.H, hk = h / p.G, Hkv = p.H / p.G;
+    auto qrow = [&](int i) { return (size_t)row_index(p.layout, b, h, i, p.H, N) * D; };
+    auto krow = [&](int j) { return (size_t)row_index(p.layout, b, hk, j, Hkv, N) * D; };
 
     for (int idx = threadIdx.x; idx < kRows * D; idx += blockDim.x) {
         const int r = idx / D, d = idx % D;
-        sq[r * ld + d] = (r0 + r < N) ? p.q[head + (size_t)(r0 + r) * D + d] : 0.f;
+        sq[r * ld + d] = (r0 + r < N) ? p.q[qrow(r0 + r) + d] : 0.f;
     }
 
     // Key range of this row block.
@@ -74,8 +76,8 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_f32_kernel(const SimtParams p
         for (int idx = threadIdx.x; idx < kKeys * D; idx += blockDim.x) {
             const int r = idx / D, d = idx % D;
             const bool in = k0 + r < N;
-            sk[r * ld + d] = in ? p.k[head + (size_t)(k0 + r) * D + d] : 0.f;
-            sv[r * D + d] = in ? p.v[head + (size_t)(k0 + r) * D + d] : 0.f;
+            sk[r * ld + d] = in ? p.k[krow(k0 + r) + d] : 0.f;
+            sv[r * D + d] = in ? p.v[krow(k0 + r) + d] : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(128) fa_fwd_simt_f32_kernel(const SimtParams p
 #pragma unroll
         for (int c = 0; c < kMaxD / 32; ++c) {
             const int d = lane + 32 * c;
-            if (d < D) p.o[head + (size_t)i * D + d] = acc[rr][c] * inv;
+            if (d < D) p.o[qrow(i) + d] = acc[rr][c] * inv;
         }
         if (lane == 0 && p.lse) p.lse[(size_t)bh * N + i] = live ? m[rr] + logf(l[rr]) : -INFINITY;
     }

@@ -192,12 +192,19 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
     bool ok = true;
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
+        const int b = un.bh / p.H, h = un.bh % p.H, hk = h / p.G;
+        // Tensor-map coordinates (d, row, head, batch), rows and heads swapped for [B,N,H,D].
+        auto load = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c, int row, int head) {
+            if (p.layout == LAYOUT_BHND)
+                tma_load_4d(dst, tm, bar, c * 64, row, head, b);
+            else
+                tma_load_4d(dst, tm, bar, c * 64, head, row, b);
+        };
         if (q_it > 0 && !(ok = W.wait(q_empty, (q_it - 1) & 1))) break;
         mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
         for (int t = 0; t < 2; ++t)
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c * 64, un.q0 + t * kTileM,
-                            un.bh);
+                load(sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c, un.q0 + t * kTileM, h);
         ++q_it;
         for (int j = un.jlo; j < un.jhi && ok; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
@@ -209,7 +216,7 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
                 mbar_arrive_expect_tx(full, C::kTileBytes);
                 const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c * 64, j * kTileN, un.bh);
+                    load(sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c, j * kTileN, hk);
                 ++kv_it;
             }
         }
@@ -527,7 +534,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
         tc_fence_after();
         const float inv = 1.f / l;
         const bool live = qi < p.g.N;
-        const size_t orow = (size_t)un.bh * p.g.N + (size_t)(live ? qi : 0);
+        const size_t orow = (size_t)row_index(p.layout, un.bh / p.H, un.bh % p.H, live ? qi : 0, p.H, p.g.N);
+        const size_t lrow = (size_t)un.bh * p.g.N + (size_t)(live ? qi : 0);
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -551,7 +559,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                 }
             }
         }
-        if (live && p.lse) p.lse[orow] = (m_ref + log2f(l)) * kLn2;
+        if (live && p.lse) p.lse[lrow] = (m_ref + log2f(l)) * kLn2;
         tc_fence_before();
         mbar_arrive(o_free);
     }

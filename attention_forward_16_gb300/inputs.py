@@ -74,11 +74,14 @@ class DecodeWorkload:
     win_l: int = -1
     win_r: int = -1
     seed: int = 0
+    Hkv: int = 0        # K/V heads (0: same as H)
 
 
 DECODE_WORKLOADS = {
     "bf16_decode_32k": DecodeWorkload("bf16_decode_32k", 8, 32, 1, 32768, 128, "bf16", 1.0 / math.sqrt(128),
                                       MASK_CAUSAL, seed=1101),
+    "bf16_decode_gqa_32k": DecodeWorkload("bf16_decode_gqa_32k", 8, 32, 1, 32768, 128, "bf16", 1.0 / math.sqrt(128),
+                                          MASK_CAUSAL, seed=1103, Hkv=8),
     "f16_decode_4k_q4": DecodeWorkload("f16_decode_4k_q4", 4, 32, 4, 4096, 128, "f16", 1.0 / math.sqrt(128),
                                        MASK_CAUSAL, seed=1102),
 }
@@ -87,7 +90,7 @@ DECODE_WORKLOADS = {
 def make_decode(w: DecodeWorkload):
     """Q [B, H, Nq, D] and the K, V cache [B, H, Nk, D] (K and V from their own stream)."""
     q, _, _ = make_qkv(w.B, w.H, w.Nq, w.D, w.dtype, seed=w.seed, n_k=1)
-    _, k, v = make_qkv(w.B, w.H, 1, w.D, w.dtype, seed=w.seed + 1, n_k=w.Nk)
+    _, k, v = make_qkv(w.B, w.Hkv or w.H, 1, w.D, w.dtype, seed=w.seed + 1, n_k=w.Nk)
     return q, k, v
 
 

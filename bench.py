@@ -405,7 +405,8 @@ def run_decode(args, w, world, rank, local, pg):
     dq, dk, dv = q.to(device), k.to(device), v.to(device)
     do = torch.empty_like(dq)
     dl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
-    ns, wb = fa.fa_decode_plan(w.B, w.H, w.Nq, w.Nk, w.D, 0)
+    Hkv = w.Hkv or w.H
+    ns, wb = fa.fa_decode_plan_gqa(w.B, w.H, Hkv, w.Nq, w.Nk, w.D, 0)
     ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=device)
     window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
     stream = torch.cuda.current_stream(device)
@@ -429,7 +430,7 @@ def run_decode(args, w, world, rank, local, pg):
     clk = clocks.stop() if clocks else None
     ms = reduce_max(pg, t0.elapsed_time(t1), device) / args.steps
     e = {"f16": 2, "bf16": 2, "f32": 4}[w.dtype]
-    nbytes = w.B * w.H * (2 * w.Nk * w.D * e + 2 * w.Nq * w.D * e + w.Nq * 4)
+    nbytes = w.B * Hkv * 2 * w.Nk * w.D * e + w.B * w.H * (2 * w.Nq * w.D * e + w.Nq * 4)
     if rank != 0:
         return 0
     peaks, src = measured_peaks()
@@ -439,9 +440,10 @@ def run_decode(args, w, world, rank, local, pg):
         "metric": "attention decode HBM GB/s (split-K, K/V cache read once)", "value": gbs * world, "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "D": w.D, "mask": w.mask,
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": Hkv, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+                   "mask": w.mask,
                    "n_splits": ns, "workspace_bytes": wb,
-                   "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * w.H * w.Nk * w.D * e >> 20)},
+                   "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * Hkv * w.Nk * w.D * e >> 20)},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "traffic": None, "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "peak_source": src},

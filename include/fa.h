@@ -48,6 +48,12 @@ enum {
                             -1 means unbounded on that side                    */
 };
 
+/* Memory layouts (fa_fwd_gqa).  BHND: contiguous [B, H, N, D].  BNHD:
+ * contiguous [B, N, H, D] -- the "[total_tokens, H, D]" per-batch layout of
+ * the Ascend C page's section 4.1 parameter struct, i.e. projection outputs
+ * used without a transposing copy. */
+enum { FA_LAYOUT_BHND = 0, FA_LAYOUT_BNHD = 1 };
+
 /* Element types of Q, K, V (and O unless fa_fwd_ex overrides it). */
 enum { FA_F16 = 0, FA_BF16 = 1, FA_F32 = 2 };
 
@@ -155,6 +161,26 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
               void* stream);
 
 /*
+ * fa_decode_plan_gqa / fa_decode_gqa -- decode with grouped K/V heads and a
+ * choice of layout.  q and o have H heads, k and v H_kv heads (H a multiple
+ * of H_kv; query head h reads K/V head h / (H / H_kv)); `layout` is
+ * FA_LAYOUT_BHND (q [B, H, Nq, D], k/v [B, H_kv, Nk, D]) or FA_LAYOUT_BNHD
+ * (q [B, Nq, H, D], k/v [B, Nk, H_kv, D]); lse is [B, H, Nq].  One CTA group
+ * serves all H / H_kv query heads of a K/V head, so the cache is read once
+ * per K/V head; (H / H_kv) * Nq must be at most 16 (FA_ERR_UNSUPPORTED
+ * otherwise).  Workspace rules and the other errors as for fa_decode, plus
+ * FA_ERR_ARG for a bad H_kv or layout.  fa_decode / fa_decode_plan are these
+ * with H_kv == H and FA_LAYOUT_BHND.
+ */
+int fa_decode_plan_gqa(int B, int H, int H_kv, int Nq, int Nk, int D, int n_splits, int* n_splits_out,
+                       unsigned long long* workspace_bytes);
+int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H, int H_kv, int Nq, int Nk, int D, float scale,
+                  int mask_kind, int win_l, int win_r, int dtype, int layout,
+                  int n_splits, void* workspace, unsigned long long workspace_bytes,
+                  void* stream);
+
+/*
  * fa_decode_noalloc -- fa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point.  It exists for code that
@@ -184,6 +210,21 @@ int fa_decode_noalloc(const void* q, const void* k, const void* v, void* o, floa
                       int mask_kind, int win_l, int win_r, int dtype, int n_splits,
                       void* stream);
 unsigned long long fa_decode_noalloc_scratch_bytes(void);
+
+/*
+ * fa_fwd_gqa -- fa_fwd_ex with grouped K/V heads and a choice of layout.
+ *
+ * Q and O have H heads, K and V have H_kv heads (1 <= H_kv <= H, H a multiple
+ * of H_kv); query head h attends with K/V head h / (H / H_kv) (grouped-query
+ * attention; H_kv == H is ordinary multi-head attention).  `layout` is
+ * FA_LAYOUT_BHND or FA_LAYOUT_BNHD for all of Q, K, V and O; LSE is always
+ * [B, H, N].  Same element types, head dimensions, masks, alignment and error
+ * codes as fa_fwd_ex, plus FA_ERR_ARG for a bad H_kv or layout.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int H_kv, int N, int D, float scale,
+               int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout,
+               void* stream);
 
 /*
  * fa_device_status -- synchronise `stream`, then report and clear the

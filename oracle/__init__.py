@@ -31,6 +31,7 @@ from .attention import (  # noqa: F401
     allowed_mask,
     attention_probs,
     attention_three_pass,
+    attention_grouped,
     attention_online,
     attention_bruteforce,
     unmasked_pairs,

@@ -139,6 +139,23 @@ def attention_three_pass(q, k, v, scale, mask_kind=MASK_NONE, win_l=-1, win_r=-1
     return o, lse
 
 
+def attention_grouped(q, k, v, scale, mask_kind=MASK_NONE, win_l=-1, win_r=-1, q_offset=0):
+    """Grouped-query attention: q [B, H, Nq, D], k and v [B, H_kv, Nk, D] with
+    H a multiple of H_kv; query head h uses key/value head h // (H // H_kv).
+    Each head is the plain definition of :func:`attention_three_pass`."""
+    H, Hkv = q.shape[1], k.shape[1]
+    if Hkv < 1 or H % Hkv:
+        raise ValueError("H must be a multiple of H_kv")
+    G = H // Hkv
+    outs_o, outs_l = [], []
+    for h in range(H):
+        o, lse = attention_three_pass(q[:, h:h + 1], k[:, h // G:h // G + 1], v[:, h // G:h // G + 1], scale,
+                                      mask_kind, win_l, win_r, q_offset)
+        outs_o.append(o)
+        outs_l.append(lse)
+    return np.concatenate(outs_o, axis=1), np.concatenate(outs_l, axis=1)
+
+
 def attention_online(q, k, v, scale, mask_kind=MASK_NONE, win_l=-1, win_r=-1,
                      q_offset=0, block_k=64):
     """The online-softmax recurrence over blocks of keys, in float64.

@@ -123,3 +123,41 @@ def test_decode_workspace_errors():
     torch.cuda.synchronize()
     ns1, wb1 = fb.fa_decode_plan(1, 2, 1, 5000, 64, 1)
     assert ns1 == 1 and wb1 == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+@pytest.mark.parametrize("H,Hkv,Nq", [(8, 8, 2), (8, 2, 2), (8, 1, 1), (16, 1, 1)])
+@pytest.mark.parametrize("Nk", [999, 3000])
+def test_decode_grouped_heads_and_layouts(dtype, layout, H, Hkv, Nq, Nk):
+    from oracle import attention_grouped
+    B, D = 2, 128
+    q, _, _ = make_qkv(B, H, Nq, D, dtype, seed=900 + Hkv, n_k=1)
+    _, k, v = make_qkv(B, Hkv, 1, D, dtype, seed=901 + Hkv, n_k=Nk)
+    perm = (lambda t: t.permute(0, 2, 1, 3).contiguous()) if layout == "bnhd" else (lambda t: t)
+    for mk, wl, wr in MASKS:
+        for ns in (0, 1, 7):
+            window = (wl, wr) if mk == MASK_WINDOW else None
+            o, lse = fa.attention_decode(perm(q).cuda(), perm(k).cuda(), perm(v).cuda(), scale=0.1,
+                                         causal=mk == MASK_CAUSAL, window=window, n_splits=ns, layout=layout)
+            torch.cuda.synchronize()
+            o = perm(o.cpu()).float().numpy().astype(np.float64)
+            ro, rlse = attention_grouped(q.double().numpy(), k.double().numpy(), v.double().numpy(), 0.1, mk, wl, wr,
+                                         q_offset=Nk - Nq)
+            err = np.abs(o - ro)
+            what = f"{dtype} {layout} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} mask={mk} splits={ns}"
+            if dtype == "f32":
+                assert err.max() <= 1e-5, what
+            else:
+                assert (err - _half_ulp(ro, dtype)).max() <= 5e-5, what
+            assert np.abs(lse.cpu().numpy() - rlse).max() <= 1e-5, what
+
+
+def test_decode_grouped_rejects_too_many_rows():
+    q = torch.zeros(1, 32, 1, 128, dtype=torch.float16, device="cuda")
+    p = q.data_ptr()
+    # 32 query heads on one K/V head: 32 rows per group > 16
+    assert fb.fa_decode_gqa(p, p, p, p, None, 1, 32, 1, 1, 64, 128, 0.1, 0, -1, -1, fb.FA_F16, 0, 1, None, 0,
+                            None) == fb.FA_ERR_UNSUPPORTED
+    assert fb.fa_decode_gqa(p, p, p, p, None, 1, 32, 5, 1, 64, 128, 0.1, 0, -1, -1, fb.FA_F16, 0, 1, None, 0,
+                            None) == fb.FA_ERR_ARG

@@ -315,3 +315,60 @@ def test_full_size_sampled_heads(name):
                                         vd[b:b + 1, h:h + 1], w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
         _check(o[b:b + 1, h:h + 1, r0:r0 + 64].astype(np.float64), lse[b:b + 1, h:h + 1, r0:r0 + 64].astype(np.float64),
                ro, rlse, w.dtype, False, f"{name} rows {r0}.. of head {(b, h)}")
+
+
+# ------------------------------------------- layouts and grouped K/V heads
+
+def _to_bhnd(x, layout):
+    return x if layout == "bhnd" else x.permute(0, 2, 1, 3).contiguous()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+@pytest.mark.parametrize("Hkv", [6, 3, 1])
+@pytest.mark.parametrize("D,N", [(64, 300), (128, 129)])
+def test_layouts_and_grouped_heads(dtype, layout, Hkv, D, N):
+    from oracle import attention_grouped
+    B, H = 2, 6
+    q, _, _ = make_qkv(B, H, N, D, dtype, seed=500 + Hkv)
+    _, k, v = make_qkv(B, Hkv, N, D, dtype, seed=600 + Hkv)
+    if layout == "bnhd":
+        q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))
+    for mk, wl, wr in [(MASK_NONE, -1, -1), (MASK_CAUSAL, -1, -1), (MASK_WINDOW, 70, 3)]:
+        window = (wl, wr) if mk == MASK_WINDOW else None
+        o, lse = fa.attention_fwd(q.cuda(), k.cuda(), v.cuda(), scale=0.1, causal=mk == MASK_CAUSAL, window=window,
+                                  o_dtype=torch.float32, layout=layout)
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        assert o.shape == q.shape and lse.shape == (B, H, N)
+        ro, rlse = attention_grouped(_to_bhnd(q, layout).double().numpy(), _to_bhnd(k, layout).double().numpy(),
+                                     _to_bhnd(v, layout).double().numpy(), 0.1, mk, wl, wr)
+        _check(_to_bhnd(o.cpu(), layout).numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rlse,
+               dtype, True, f"{layout} Hkv={Hkv} D={D} N={N} mask={mk}")
+
+
+def test_bnhd_benchmark_shape_sampled():
+    """[B, N, H, D] input at the benchmark size (no transposing copy) with
+    GQA 32 -> 8, checked on sampled heads."""
+    from oracle import attention_grouped
+    B, N, H, Hkv, D = 4, 4096, 32, 8, 128
+    q, _, _ = make_qkv(B, H, N, D, "f16", seed=700)
+    _, k, v = make_qkv(B, Hkv, N, D, "f16", seed=701)
+    qb, kb, vb = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))
+    o, lse = fa.attention_fwd(qb.cuda(), kb.cuda(), vb.cuda(), causal=True, layout="bnhd")
+    torch.cuda.synchronize()
+    o = o.float().cpu().permute(0, 2, 1, 3).numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    for b, h in [(0, 0), (1, 13), (3, 31)]:
+        ro, rlse = attention_grouped(q[b:b + 1, h:h + 1].double().numpy(),
+                                     k[b:b + 1, h // 4:h // 4 + 1].double().numpy(),
+                                     v[b:b + 1, h // 4:h // 4 + 1].double().numpy(), 1 / math.sqrt(D), MASK_CAUSAL)
+        _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rlse, "f16", False, f"bnhd gqa head {(b, h)}")
+
+
+def test_gqa_rejects_bad_head_counts():
+    q = torch.zeros(1, 6, 64, 64, dtype=torch.float16, device="cuda")
+    p = q.data_ptr()
+    assert fb.fa_fwd_gqa(p, p, p, p, None, 1, 6, 4, 64, 64, 0.1, 0, -1, -1, fb.FA_F16, fb.FA_F16, 0, None) == fb.FA_ERR_ARG
+    assert fb.fa_fwd_gqa(p, p, p, p, None, 1, 6, 7, 64, 64, 0.1, 0, -1, -1, fb.FA_F16, fb.FA_F16, 0, None) == fb.FA_ERR_ARG
+    assert fb.fa_fwd_gqa(p, p, p, p, None, 1, 6, 3, 64, 64, 0.1, 0, -1, -1, fb.FA_F16, fb.FA_F16, 2, None) == fb.FA_ERR_ARG

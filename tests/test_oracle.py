@@ -321,3 +321,28 @@ def _planted(kind):
 def test_pins_catch_planted_mistakes(kind):
     with pytest.raises(AssertionError):
         _check_hand(_planted(kind))
+
+
+# ------------------------------------------------------- grouped K/V heads
+
+def test_grouped_equals_plain_with_repeated_kv_heads():
+    from oracle import attention_grouped
+    q = _rand((2, 6, 19, 8), 1)
+    k, v = _rand((2, 2, 19, 8), 2), _rand((2, 2, 19, 8), 3)
+    for mask, wl, wr in MASKS[:4]:
+        o, lse = attention_grouped(q, k, v, 0.4, mask, wl, wr)
+        ro, rlse = attention_three_pass(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), 0.4, mask, wl, wr)
+        np.testing.assert_array_equal(o, ro)
+        np.testing.assert_array_equal(lse, rlse)
+    with pytest.raises(ValueError):
+        attention_grouped(q, k[:, :1].repeat(4, axis=1), v[:, :1].repeat(4, axis=1), 0.4)
+
+
+def test_grouped_head_mapping_is_contiguous_groups():
+    """Query heads 0..G-1 share K/V head 0 (not heads 0, Hkv, 2 Hkv, ...)."""
+    from oracle import attention_grouped
+    q = _rand((1, 4, 5, 3), 4)
+    k = np.stack([np.full((5, 3), 0.0), np.full((5, 3), 0.0)])[None]
+    v = np.stack([np.full((5, 3), 1.0), np.full((5, 3), 2.0)])[None]
+    o, _ = attention_grouped(q, k, v, 1.0)
+    np.testing.assert_array_equal(o[0, :, 0, 0], [1.0, 1.0, 2.0, 2.0])
