@@ -122,10 +122,10 @@ struct Waiter {
     // Bounded wait on one phase.  False on timeout (recorded) or if another
     // role already aborted.
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_nohint(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_nohint(bar, parity)) return true;
             if ((it & 15u) == 0) {
                 if (*abort) return false;
                 if (globaltimer_ns() - t0 > limit) {
@@ -268,7 +268,6 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         if (*other_progress >= target) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-            __nanosleep(20);
             if (*other_progress >= target) return true;
             if ((it & 15u) == 0) {
                 if (*W.abort) return false;
