@@ -19,6 +19,10 @@ FlashAttention reproduces exactly:
   practice", section "The core idea of FlashAttention: IO-aware"
   (``standard_attention``: matmul, softmax over the last axis, matmul).
 
+``rope.py`` adds the rotary position embedding that the first page's
+section 9 ("Extensions: integration with RoPE and a paged KV cache") says
+is applied to the Q and K blocks as they are loaded.
+
 Every function here is pinned by ``tests/test_oracle.py`` against something
 other than itself (brute force in exact arithmetic, closed forms, invariants,
 a foreign library).  No function is "parity unpinned".
@@ -35,4 +39,12 @@ from .attention import (  # noqa: F401
     attention_online,
     attention_bruteforce,
     unmasked_pairs,
+)
+from .rope import (  # noqa: F401
+    STYLE_HALF,
+    STYLE_INTERLEAVED,
+    apply_rope,
+    attention_rope,
+    pair_index,
+    rope_tables,
 )
