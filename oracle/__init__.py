@@ -19,7 +19,9 @@ FlashAttention reproduces exactly:
   practice", section "The core idea of FlashAttention: IO-aware"
   (``standard_attention``: matmul, softmax over the last axis, matmul).
 
-``rope.py`` adds the rotary position embedding that the first page's
+``backward.py`` gives the gradients of that definition with respect to Q, K
+and V (the chain rule through it), for the backward pass the second page
+says the operator also has.  ``rope.py`` adds the rotary position embedding that the first page's
 section 9 ("Extensions: integration with RoPE and a paged KV cache") says
 is applied to the Q and K blocks as they are loaded.
 
@@ -40,6 +42,7 @@ from .attention import (  # noqa: F401
     attention_bruteforce,
     unmasked_pairs,
 )
+from .backward import attention_backward, attention_backward_grouped  # noqa: F401
 from .rope import (  # noqa: F401
     STYLE_HALF,
     STYLE_INTERLEAVED,
