@@ -24,6 +24,8 @@ _LAYOUT_CODE = {"bhnd": FA_LAYOUT_BHND, "bnhd": FA_LAYOUT_BNHD}
 FA_F16, FA_BF16, FA_F32 = 0, 1, 2
 FA_OK, FA_ERR_ARG, FA_ERR_UNSUPPORTED, FA_ERR_ALIGN, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
 FA_ERR_SCRATCH = -7
+FA_ROPE_HALF, FA_ROPE_INTERLEAVED = 0, 1
+_ROPE_STYLE = {"half": FA_ROPE_HALF, "interleaved": FA_ROPE_INTERLEAVED}
 
 _DTYPE_CODE = {torch.float16: FA_F16, torch.bfloat16: FA_BF16, torch.float32: FA_F32}
 
@@ -46,6 +48,11 @@ SIGNATURES = {
                            ctypes.c_ulonglong, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
     "fa_decode_noalloc_scratch_bytes": (ctypes.c_ulonglong, []),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P,
+                    ctypes.c_ulonglong, _P]),
+    "fa_bwd_workspace_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]),
+    "fa_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "fa_rope_tables": (_I, [_P, _P, _I, _I, ctypes.c_double, _P]),
     "fa_device_status": (_I, [_P]),
     "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
@@ -157,6 +164,29 @@ def fa_decode_noalloc_scratch_bytes():
 def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, layout, stream):
     return load().fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype,
                              layout, stream)
+
+
+def fa_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, layout,
+           workspace, workspace_bytes, stream):
+    return load().fa_bwd(q, k, v, o, d_o, lse, dq, dk, dv, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype,
+                         layout, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_bytes(B, H, N):
+    """Workspace bytes fa_bwd needs; raises on bad sizes."""
+    out = ctypes.c_ulonglong(0)
+    _check(load().fa_bwd_workspace_bytes(B, H, N, ctypes.byref(out)), "fa_bwd_workspace_bytes")
+    return out.value
+
+
+def fa_rope(q, k, q_out, k_out, cos_tab, sin_tab, B, H, H_kv, Nq, Nk, D, q_pos0, k_pos0, n_pos, style, dtype,
+            layout, stream):
+    return load().fa_rope(q, k, q_out, k_out, cos_tab, sin_tab, B, H, H_kv, Nq, Nk, D, q_pos0, k_pos0, n_pos,
+                          style, dtype, layout, stream)
+
+
+def fa_rope_tables(cos_tab, sin_tab, n_pos, D, base, stream):
+    return load().fa_rope_tables(cos_tab, sin_tab, n_pos, D, base, stream)
 
 
 def fa_device_status(stream=None):
@@ -291,6 +321,120 @@ def attention_decode(q, k, v, scale=None, causal=False, window=None, n_splits=0,
                            workspace.numel() if workspace is not None else 0, s)
     _check(rc, "fa_decode_gqa")
     return out, lse
+
+
+def attention_bwd(q, k, v, o, lse, d_o, scale=None, causal=False, window=None, layout="bhnd", dq=None, dk=None,
+                  dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of attention_fwd for an upstream gradient ``d_o``.
+
+    q, k, v, o, lse are the forward's inputs and outputs (O in the inputs'
+    16-bit type), d_o has O's shape; the mask and scale must be the forward's.
+    The gradients are allocated with torch unless given; the workspace too
+    (a CUDA uint8 tensor of at least ``fa_bwd_workspace_bytes`` bytes).
+    Returns (dq, dk, dv)."""
+    if layout not in _LAYOUT_CODE:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
+    for t in (q, k, v, o, d_o):
+        if t.dim() != 4 or not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, d_o must be contiguous 4-D CUDA tensors of one dtype")
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("the backward pass takes float16 or bfloat16")
+    if o.shape != q.shape or d_o.shape != q.shape or v.shape != k.shape:
+        raise ValueError("o and d_o must have q's shape, v k's")
+    if layout == "bhnd":
+        B, H, N, D = q.shape
+        Hkv = k.shape[1]
+    else:
+        B, N, H, D = q.shape
+        Hkv = k.shape[2]
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be the forward's contiguous fp32 [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mk, wl, wr = mask_args(causal, window)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        wb = fa_bwd_workspace_bytes(B, H, N)
+        if workspace is None:
+            workspace = torch.empty(wb, dtype=torch.uint8, device=q.device)
+        s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), d_o.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, D, float(scale), mk, wl, wr,
+                    _DTYPE_CODE[q.dtype], _LAYOUT_CODE[layout], workspace.data_ptr(), workspace.numel(), s)
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def rope_tables(n_pos, D, base=10000.0, device="cuda", stream=None):
+    """cos, sin fp32 [n_pos, D/2] CUDA tensors for positions 0 .. n_pos-1,
+    filled by ``fa_rope_tables`` (angle p * base^(-2i/D))."""
+    dev = torch.device(device)
+    cos = torch.empty((n_pos, D // 2), dtype=torch.float32, device=dev)
+    sin = torch.empty_like(cos)
+    with torch.cuda.device(dev):
+        s = (stream or torch.cuda.current_stream(dev)).cuda_stream
+        rc = fa_rope_tables(cos.data_ptr(), sin.data_ptr(), n_pos, D, float(base), s)
+    _check(rc, "fa_rope_tables")
+    return cos, sin
+
+
+def apply_rope(q=None, k=None, cos=None, sin=None, style="half", q_pos0=0, k_pos0=0, layout="bhnd",
+               q_out=None, k_out=None, inplace=False, stream=None):
+    """Rotary position embedding of q and/or k with ``fa_rope``.
+
+    q is [B, H, Nq, D] (``layout="bhnd"``) or [B, Nq, H, D] (``"bnhd"``), k
+    likewise with H_kv heads; row n of q sits at position q_pos0 + n, of k at
+    k_pos0 + n.  ``cos``/``sin`` are fp32 [n_pos, D/2] CUDA tensors
+    (``rope_tables``).  ``style``: "half" pairs (i, i + D/2), "interleaved"
+    pairs (2i, 2i + 1).  Returns (q_rot, k_rot), None for a tensor not given;
+    ``inplace=True`` rotates the given tensors themselves.
+    """
+    if style not in _ROPE_STYLE:
+        raise ValueError(f"style must be one of {sorted(_ROPE_STYLE)}")
+    if layout not in _LAYOUT_CODE:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
+    if q is None and k is None:
+        raise ValueError("give q, k or both")
+    ref = q if q is not None else k
+    if cos is None or sin is None or cos.dtype != torch.float32 or sin.shape != cos.shape or cos.dim() != 2:
+        raise ValueError("cos and sin must be fp32 [n_pos, D/2] tensors of one shape")
+    for t in (q, k):
+        if t is not None and (t.dim() != 4 or not t.is_cuda or not t.is_contiguous() or t.dtype != ref.dtype
+                              or t.dtype not in _DTYPE_CODE):
+            raise ValueError("q and k must be contiguous 4-D CUDA tensors of one dtype")
+    if not (cos.is_cuda and sin.is_cuda and cos.is_contiguous() and sin.is_contiguous()):
+        raise ValueError("cos and sin must be contiguous CUDA tensors")
+    seq, head = (2, 1) if layout == "bhnd" else (1, 2)
+    B, D = ref.shape[0], ref.shape[3]
+    if q is not None and k is not None and (k.shape[0] != B or k.shape[3] != D):
+        raise ValueError("q and k disagree on B or D")
+    if cos.shape[1] != D // 2:
+        raise ValueError(f"table has {cos.shape[1]} columns, D/2 = {D // 2}")
+    H, Nq = (q.shape[head], q.shape[seq]) if q is not None else (1, 1)
+    Hkv, Nk = (k.shape[head], k.shape[seq]) if k is not None else (1, 1)
+    if q is not None and q_out is None:
+        q_out = q if inplace else torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = k if inplace else torch.empty_like(k)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    with torch.cuda.device(ref.device):
+        s = (stream or torch.cuda.current_stream(ref.device)).cuda_stream
+        rc = fa_rope(ptr(q), ptr(k), ptr(q_out), ptr(k_out), cos.data_ptr(), sin.data_ptr(), B, H, Hkv, Nq, Nk, D,
+                     int(q_pos0), int(k_pos0), cos.shape[0], _ROPE_STYLE[style], _DTYPE_CODE[ref.dtype],
+                     _LAYOUT_CODE[layout], s)
+    _check(rc, "fa_rope")
+    return q_out, k_out
+
+
+def attention_fwd_rope(q, k, v, cos, sin, style="half", pos0=0, layout="bhnd", **kw):
+    """attention_fwd on rotary-embedded q and k: ``fa_rope`` writes the
+    rotated copies (rows at positions pos0, pos0 + 1, ...), then the fused
+    forward runs on them.  Returns (O, LSE)."""
+    qr, kr = apply_rope(q, k, cos, sin, style=style, q_pos0=pos0, k_pos0=pos0, layout=layout,
+                        stream=kw.get("stream"))
+    return attention_fwd(qr, kr, v, layout=layout, **kw)
 
 
 def attention_fwd_host(q, k, v, device="cuda", **kw):

@@ -355,6 +355,127 @@ int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, 
                          n_splits, workspace, workspace_bytes, stream);
 }
 
+namespace {
+// Padded rows and the workspace split of the backward pass: LSE*log2(e) then
+// Dsum, each [B*H, Npad] fp32 on a 256-byte boundary.
+long long bwd_npad(int N) { return ((long long)N + fa::kTileM - 1) / fa::kTileM * fa::kTileM; }
+unsigned long long bwd_vec_bytes(int B, int H, int N) {
+    return ((unsigned long long)B * H * bwd_npad(N) * 4 + 255) / 256 * 256;
+}
+}  // namespace
+
+int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes) {
+    if (B <= 0 || H <= 0 || N <= 0 || !bytes) return FA_ERR_ARG;
+    *bytes = 2 * bwd_vec_bytes(B, H, N);
+    return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int H_kv, int N, int D, float scale, int mask_kind, int win_l,
+           int win_r, int dtype, int layout, void* workspace, unsigned long long workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA_ERR_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || D <= 0) return FA_ERR_ARG;
+    if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    fa::Geom g;
+    int rc = normalise_mask(mask_kind, win_l, win_r, N, &g);
+    if (rc != FA_OK) return rc;
+    const long long n_tiles = bwd_npad(N) / fa::kTileM;
+    if ((long long)B * H * n_tiles > 0x7fffffffLL) return FA_ERR_ARG;
+    if ((dtype != FA_F16 && dtype != FA_BF16) || (D != 64 && D != 128)) return FA_ERR_UNSUPPORTED;
+    const void* p16[] = {q, k, v, o, d_o, dq, dk, dv};
+    for (const void* ptr : p16)
+        if (!aligned(ptr, 16)) return FA_ERR_ALIGN;
+    if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+    const unsigned long long vb = bwd_vec_bytes(B, H, N);
+    if (!workspace || workspace_bytes < 2 * vb) return FA_ERR_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+    DeviceInfo* dev;
+    if ((rc = device_info(&dev)) != FA_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == FA_BF16;
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = make_map(&p.tm_q, q, bf16, layout, B, H, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
+    if ((rc = make_map(&p.tm_do, d_o, bf16, layout, B, H, N, D)) != FA_OK) return rc;
+    float* lse2 = static_cast<float*>(workspace);
+    float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + vb);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.lse2 = lse2;
+    p.dsum = dsum;
+    p.g = g;
+    p.H = H;
+    p.G = H / H_kv;
+    p.Hkv = H_kv;
+    p.layout = layout;
+    p.Npad = (int)bwd_npad(N);
+    p.n_tiles = (int)n_tiles;
+    p.scale = scale;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.status = dev->status;
+    cudaError_t e = fa::launch_bwd_pre(o, d_o, lse, lse2, dsum, B, H, N, p.Npad, D, layout, dtype, dev->sms, s);
+    if (e == cudaSuccess) e = fa::launch_bwd(p, B, D, bf16, s);
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_rope(const void* q, const void* k, void* q_out, void* k_out, const float* cos_tab, const float* sin_tab,
+            int B, int H, int H_kv, int Nq, int Nk, int D, int q_pos0, int k_pos0, int n_pos, int style, int dtype,
+            int layout, void* stream) {
+    if (!q && !k) return FA_ERR_ARG;
+    if ((q == nullptr) != (q_out == nullptr) || (k == nullptr) != (k_out == nullptr)) return FA_ERR_ARG;
+    if (!cos_tab || !sin_tab) return FA_ERR_ARG;
+    if (B <= 0 || D <= 0 || D % 16 != 0 || D > 1024 || n_pos <= 0) return FA_ERR_ARG;
+    if (style != fa::ROPE_HALF && style != fa::ROPE_INTERLEAVED) return FA_ERR_ARG;
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
+    if (q && (H <= 0 || Nq <= 0 || q_pos0 < 0 || (long long)q_pos0 + Nq > n_pos)) return FA_ERR_ARG;
+    if (k && (H_kv <= 0 || Nk <= 0 || k_pos0 < 0 || (long long)k_pos0 + Nk > n_pos)) return FA_ERR_ARG;
+    if (dtype < FA_F16 || dtype > FA_F32) return FA_ERR_UNSUPPORTED;
+    if ((q && (!aligned(q, 16) || !aligned(q_out, 16))) || (k && (!aligned(k, 16) || !aligned(k_out, 16))) ||
+        !aligned(cos_tab, 16) || !aligned(sin_tab, 16))
+        return FA_ERR_ALIGN;
+    DeviceInfo* dev;
+    int rc = device_info(&dev);
+    if (rc != FA_OK) return rc;
+    fa::RopeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x[0] = q;
+    p.y[0] = q_out;
+    p.n[0] = q ? Nq : 0;
+    p.heads[0] = q ? H : 0;
+    p.pos0[0] = q_pos0;
+    p.x[1] = k;
+    p.y[1] = k_out;
+    p.n[1] = k ? Nk : 0;
+    p.heads[1] = k ? H_kv : 0;
+    p.pos0[1] = k_pos0;
+    p.cos = cos_tab;
+    p.sin = sin_tab;
+    p.B = B;
+    p.D = D;
+    p.style = style;
+    p.layout = layout;
+    cudaError_t e = fa::launch_rope(p, dtype, dev->sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_rope_tables(float* cos_tab, float* sin_tab, int n_pos, int D, double base, void* stream) {
+    if (!cos_tab || !sin_tab || n_pos <= 0 || D <= 0 || D % 2 != 0 || D > 1024) return FA_ERR_ARG;
+    if (!(base > 0.0) || !std::isfinite(base)) return FA_ERR_ARG;
+    if (!aligned(cos_tab, 16) || !aligned(sin_tab, 16)) return FA_ERR_ALIGN;
+    DeviceInfo* dev;
+    int rc = device_info(&dev);
+    if (rc != FA_OK) return rc;
+    cudaError_t e = fa::launch_rope_tables(cos_tab, sin_tab, n_pos, D, base, dev->sms,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int* out, int cap) {
     if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_ARG;
     fa::Geom g;

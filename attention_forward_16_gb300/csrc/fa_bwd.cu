@@ -1,0 +1,604 @@
+// Tensor-core attention backward for sm_103a (fp16 / bf16 in, fp32 accumulate).
+//
+// The gradient of the attention definition of "Ascend C advanced practice:
+// high-performance FlashAttention-2-style tile-level fused attention"
+// (section 1.1), for the backward pass the ops-transformer walk-through says
+// the operator also has.  With P = exp(scale * S - LSE) recomputed from the
+// forward's LSE, and Dsum_i = rowsum(dO_i * O_i) (= rowsum(P * dP)):
+//
+//     dV = P^T dO      dP = dO V^T      dS = P * (dP - Dsum)
+//     dK = scale * dS^T Q                dQ = scale * dS K
+//
+// Three kernels, no atomics, deterministic:
+//   pre   one pass over O and dO: Dsum and LSE * log2(e) per row, padded to
+//         whole 128-row tiles (HBM-bound);
+//   dkdv  one CTA per (b, K/V head, 128-key tile): K and V stay in shared
+//         memory, the query tiles of every query head of the group stream
+//         through a TMA ring; TMEM holds S^T | dP^T | dV | dK;
+//   dq    one CTA per (b, head, 128-row query tile): Q and dO stay, K/V
+//         tiles stream; TMEM holds S | dP | dQ.
+// The dq kernel recomputes S and dP rather than adding partial dQ tiles with
+// atomics from the dkdv kernel: two more products per tile pair, in exchange
+// for a deterministic result and no read-modify-write traffic in L2.
+//
+// Warp roles in both kernels (256 threads): warp 0 issues TMA loads, warp 1
+// allocates TMEM and one of its threads issues tcgen05.mma, warps 4-7 turn
+// scores into P and dS (one TMEM lane = one row per thread) and write the
+// result; warps 2-3 only take part in the CTA barriers.  Every mbarrier
+// wait is bounded, as in the forward kernel.
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kWarpTmaB = 0;
+constexpr int kWarpMmaB = 1;
+constexpr int kWarpEw0 = 4;  // first of the four elementwise warps
+constexpr float kLog2e = 1.4426950408889634074f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kChunks = D / 64;                   // 128-byte column chunks per row
+    static constexpr int kBoxBytes = kTileM * 64 * 2;        // one TMA box: 128 rows x 64 elements
+    static constexpr int kTileBytes = kChunks * kBoxBytes;   // 128 rows x D
+    static constexpr int kVecBytes = kTileM * 4;             // 128 fp32 per-row values
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    // dkdv ring stage: Q tile | dO tile | LSE*log2e | Dsum (a multiple of 1024 bytes)
+    static constexpr int kStageKV = 2 * kTileBytes + 1024;
+    // dq ring stage: K tile | V tile
+    static constexpr int kStageQ = 2 * kTileBytes;
+    static constexpr int kColS = 0;
+    static constexpr int kColDP = 128;
+    static constexpr int kColA = 256;       // dV (dkdv) or dQ (dq)
+    static constexpr int kColB = 256 + D;   // dK (dkdv)
+    static constexpr int kTmemCols = 512;
+};
+
+struct __align__(16) BwdCtl {
+    uint64_t fixed_full;
+    uint64_t ring_full[4], ring_empty[4];
+    uint64_t s_full, s_free, dp_full, p_full, ds_full, acc_done, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+constexpr int dkdv_smem_bytes() {
+    return 2 * BwdCfg<D>::kTileBytes + BwdCfg<D>::kStages * BwdCfg<D>::kStageKV + (int)sizeof(BwdCtl) + 1024;
+}
+template <int D>
+constexpr int dq_smem_bytes() {
+    return 2 * BwdCfg<D>::kTileBytes + BwdCfg<D>::kStages * BwdCfg<D>::kStageQ + (int)sizeof(BwdCtl) + 1024;
+}
+static_assert(dkdv_smem_bytes<128>() <= 227 * 1024 && dq_smem_bytes<128>() <= 227 * 1024, "smem (D=128)");
+static_assert(dkdv_smem_bytes<64>() <= 227 * 1024 && dq_smem_bytes<64>() <= 227 * 1024, "smem (D=64)");
+
+// 4-D tensor-map load of one 128-row tile (all D columns): coordinates
+// (d, row, head, batch), rows and heads swapped for [B, N, H, D].
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int layout, int b,
+                                          int head, int row) {
+#pragma unroll
+    for (int c = 0; c < BwdCfg<D>::kChunks; ++c) {
+        if (layout == LAYOUT_BHND)
+            tma_load_4d(dst + c * BwdCfg<D>::kBoxBytes, tm, bar, c * 64, row, head, b);
+        else
+            tma_load_4d(dst + c * BwdCfg<D>::kBoxBytes, tm, bar, c * 64, head, row, b);
+    }
+}
+
+// Products shared by both kernels.  A tiles are K-major 128 x D (TMA boxes
+// with the 128-byte swizzle); "MN-major" B tiles are the same boxes read as
+// [K = 128 rows] x [N = D columns].
+template <int D, bool kBf16>
+struct Mma {
+    static constexpr uint32_t kIdescRows = make_idesc(kBf16, kTileM, kTileN, false);  // 128 x 128, K = D
+    static constexpr uint32_t kIdescCols = make_idesc(kBf16, kTileM, D, true);         // 128 x D, K = 128
+    // dst[128 x 128] = A[128 x D] B[128 x D]^T, both from shared memory.
+    static __device__ __forceinline__ void rows(uint32_t dst, uint32_t a, uint32_t b) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * BwdCfg<D>::kBoxBytes + (kk % 4) * 32;
+            mma_ss(dst, make_sdesc(a + off, 16, 1024), make_sdesc(b + off, 16, 1024), kIdescRows, kk > 0);
+        }
+    }
+    // dst[128 x D] (+)= T[128 x 128] (16-bit, TMEM columns at `t`) B[128 x D].
+    static __device__ __forceinline__ void cols(uint32_t dst, uint32_t t, uint32_t b, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+            const uint64_t bd = make_sdesc(b + kk * 2048, BwdCfg<D>::kBoxBytes, 1024);
+            mma_ts(dst, t + kk * 8, bd, kIdescCols, (acc || kk > 0) ? 1u : 0u);
+        }
+    }
+};
+
+__device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count) {
+    mbar_init(smem_u32(&sh->fixed_full), 1);
+    for (int s = 0; s < 4; ++s) {
+        mbar_init(smem_u32(&sh->ring_full[s]), 1);
+        mbar_init(smem_u32(&sh->ring_empty[s]), ring_empty_count);
+    }
+    mbar_init(smem_u32(&sh->s_full), 1);
+    mbar_init(smem_u32(&sh->s_free), 128);
+    mbar_init(smem_u32(&sh->dp_full), 1);
+    mbar_init(smem_u32(&sh->p_full), 128);
+    mbar_init(smem_u32(&sh->ds_full), 128);
+    mbar_init(smem_u32(&sh->acc_done), 1);
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+}
+
+// One 128-column row of fp32 values from TMEM into registers.
+__device__ __forceinline__ void ld_row128(uint32_t t, uint32_t (&r)[4][32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(t + c * 32, r[c]);
+    tmem_wait_ld();
+}
+
+// Store a thread's row of a 16-bit gradient (fp32 in TMEM, times `mul`).
+template <int D, bool kBf16>
+__device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, float mul, bool live) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t + c * 32, v);
+        tmem_wait_ld();
+        if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pack2<kBf16>(u2f(v[8 * i]) * mul, u2f(v[8 * i + 1]) * mul),
+                                    pack2<kBf16>(u2f(v[8 * i + 2]) * mul, u2f(v[8 * i + 3]) * mul),
+                                    pack2<kBf16>(u2f(v[8 * i + 4]) * mul, u2f(v[8 * i + 5]) * mul),
+                                    pack2<kBf16>(u2f(v[8 * i + 6]) * mul, u2f(v[8 * i + 7]) * mul));
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void zero_row(void* out, size_t row) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+}
+
+// ===================================================================== dK, dV
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using C = BwdCfg<D>;
+    using M = Mma<D, kBf16>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sK = smem_u32(smem);
+    const uint32_t sV = sK + C::kTileBytes;
+    const uint32_t sRing = sV + C::kTileBytes;
+    BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + 2 * C::kTileBytes + C::kStages * C::kStageKV);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA -> (b, K/V head, key tile j); consecutive CTAs share a head, so the
+    // query tiles they all stream stay in L2
+    const int j = blockIdx.x % p.n_tiles;
+    const int bk = blockIdx.x / p.n_tiles;
+    const int b = bk / p.Hkv, hk = bk % p.Hkv;
+    int ilo, ihi;
+    q_tile_range(p.g, j, ilo, ihi);
+    const int ni = ihi - ilo;
+    const int n_items = ni * p.G;  // (query head of the group, query tile) pairs, head-major
+
+    if (threadIdx.x == 0) init_ctl(sh, 1);
+    if (warp == kWarpMmaB) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
+    auto item = [&](int n, int& h, int& i) {
+        h = hk * p.G + n / ni;
+        i = ilo + n % ni;
+    };
+
+    if (warp == kWarpTmaB && lane == 0 && n_items > 0) {
+        // ------------------------------------------------------------ TMA
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_do);
+        const uint32_t fixed = smem_u32(&sh->fixed_full);
+        mbar_arrive_expect_tx(fixed, 2 * C::kTileBytes);
+        load_tile<D>(sK, &p.tm_k, fixed, p.layout, b, hk, j * kTileN);
+        load_tile<D>(sV, &p.tm_v, fixed, p.layout, b, hk, j * kTileN);
+        bool ok = true;
+        int n = 0;
+        for (; n < n_items && ok; ++n) {
+            const int st = n % C::kStages;
+            if (n >= C::kStages && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((n / C::kStages) - 1) & 1))) break;
+            int h, i;
+            item(n, h, i);
+            const uint32_t full = smem_u32(&sh->ring_full[st]);
+            const uint32_t stage = sRing + st * C::kStageKV;
+            mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 2 * C::kVecBytes);
+            load_tile<D>(stage, &p.tm_q, full, p.layout, b, h, i * kTileM);
+            load_tile<D>(stage + C::kTileBytes, &p.tm_do, full, p.layout, b, h, i * kTileM);
+            const size_t vrow = ((size_t)b * p.H + h) * p.Npad + (size_t)i * kTileM;
+            bulk_load(stage + 2 * C::kTileBytes, p.lse2 + vrow, C::kVecBytes, full);
+            bulk_load(stage + 2 * C::kTileBytes + C::kVecBytes, p.dsum + vrow, C::kVecBytes, full);
+        }
+        // let every issued copy land before the CTA releases shared memory
+        W.drain(fixed, 0);
+        for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
+            W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
+    } else if (warp == kWarpMmaB && lane == 0 && n_items > 0) {
+        // ------------------------------------------------------------ MMA
+        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+        const uint32_t tDV = tmem + C::kColA, tDK = tmem + C::kColB;
+        auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageKV; };
+        auto ring_full = [&](int n) { return W.wait(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
+        bool ok = W.wait(smem_u32(&sh->fixed_full), 0) && ring_full(0);
+        if (ok) {
+            tc_fence_after();
+            M::rows(tS, sK, stage(0));                       // S^T = K Q^T
+            mma_commit(smem_u32(&sh->s_full));
+            M::rows(tDP, sV, stage(0) + C::kTileBytes);      // dP^T = V dO^T
+            mma_commit(smem_u32(&sh->dp_full));
+        }
+        for (int n = 0; n < n_items && ok; ++n) {
+            if (!(ok = W.wait(smem_u32(&sh->p_full), n & 1))) break;
+            tc_fence_after();
+            M::cols(tDV, tS, stage(n) + C::kTileBytes, n > 0);   // dV += P^T dO
+            if (n + 1 < n_items) {
+                if (!(ok = ring_full(n + 1))) break;
+                tc_fence_after();
+                M::rows(tS, sK, stage(n + 1));
+                mma_commit(smem_u32(&sh->s_full));
+            }
+            if (!(ok = W.wait(smem_u32(&sh->ds_full), n & 1))) break;
+            tc_fence_after();
+            M::cols(tDK, tDP, stage(n), n > 0);                  // dK += dS^T Q
+            mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
+            if (n + 1 < n_items) {
+                M::rows(tDP, sV, stage(n + 1) + C::kTileBytes);
+                mma_commit(smem_u32(&sh->dp_full));
+            }
+        }
+        mma_commit(smem_u32(&sh->acc_done));
+        mma_commit(smem_u32(&sh->drain));
+        W.drain(smem_u32(&sh->drain), 0);
+    } else if (warp >= kWarpEw0) {
+        // ------------------------------------------------- P, dS, epilogue
+        const int wq = warp - kWarpEw0;
+        const int c = wq * 32 + lane;          // key row within the tile
+        const int kc = j * kTileN + c;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS;
+        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        for (int n = 0; n < n_items && ok; ++n) {
+            int h, i;
+            item(n, h, i);
+            const uint8_t* stage = smem + 2 * C::kTileBytes + (n % C::kStages) * C::kStageKV;
+            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes);
+            const float4* dsum = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes);
+            if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
+            tc_fence_after();
+            uint32_t s[4][32];
+            ld_row128(tS, s);
+            int r_lo = 0, r_hi = kTileM - 1;
+            if (tile_needs_mask(p.g, i * kTileM, j)) key_visible_rows(p.g, kc, i, r_lo, r_hi);
+            // P^T row: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const float4 l4 = lse2[cc * 8 + v];
+                    const int q = cc * 32 + 4 * v;
+                    float e0 = ex2(fmaf(u2f(s[cc][4 * v]), c2, -l4.x));
+                    float e1 = ex2(fmaf(u2f(s[cc][4 * v + 1]), c2, -l4.y));
+                    float e2 = ex2(fmaf(u2f(s[cc][4 * v + 2]), c2, -l4.z));
+                    float e3 = ex2(fmaf(u2f(s[cc][4 * v + 3]), c2, -l4.w));
+                    if (q < r_lo || q > r_hi) e0 = 0.f;
+                    if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
+                    if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
+                    if (q + 3 < r_lo || q + 3 > r_hi) e3 = 0.f;
+                    s[cc][4 * v] = f2u(e0);
+                    s[cc][4 * v + 1] = f2u(e1);
+                    s[cc][4 * v + 2] = f2u(e2);
+                    s[cc][4 * v + 3] = f2u(e3);
+                    pk[2 * v] = pack2<kBf16>(e0, e1);
+                    pk[2 * v + 1] = pack2<kBf16>(e2, e3);
+                }
+                tmem_st16(tS + 16 * cc, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh->p_full));
+            // dS^T row: p * (dP - Dsum_q), written over the dP columns already read
+            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t d[32];
+                tmem_ld32(tDP + 32 * cc, d);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const float4 d4 = dsum[cc * 8 + v];
+                    const float g0 = u2f(s[cc][4 * v]) * (u2f(d[4 * v]) - d4.x);
+                    const float g1 = u2f(s[cc][4 * v + 1]) * (u2f(d[4 * v + 1]) - d4.y);
+                    const float g2 = u2f(s[cc][4 * v + 2]) * (u2f(d[4 * v + 2]) - d4.z);
+                    const float g3 = u2f(s[cc][4 * v + 3]) * (u2f(d[4 * v + 3]) - d4.w);
+                    pk[2 * v] = pack2<kBf16>(g0, g1);
+                    pk[2 * v + 1] = pack2<kBf16>(g2, g3);
+                }
+                tmem_st16(tDP + 16 * cc, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh->ds_full));
+        }
+        // epilogue: dV and scale * dK rows of the keys that exist
+        const bool live = kc < p.g.N;
+        const size_t row = (size_t)row_index(p.layout, b, hk, live ? kc : 0, p.Hkv, p.g.N);
+        if (n_items == 0) {
+            if (live) {
+                zero_row<D>(p.dv, row);
+                zero_row<D>(p.dk, row);
+            }
+        } else if (ok && W.wait_warp(smem_u32(&sh->acc_done), 0)) {
+            tc_fence_after();
+            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dv, row, 1.f, live);
+            store_row<D, kBf16>(tmem + lane_base + C::kColB, p.dk, row, p.scale, live);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMmaB) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ========================================================================= dQ
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using C = BwdCfg<D>;
+    using M = Mma<D, kBf16>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sDO = sQ + C::kTileBytes;
+    const uint32_t sRing = sDO + C::kTileBytes;
+    BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + 2 * C::kTileBytes + C::kStages * C::kStageQ);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA -> (b, head, query tile i); consecutive CTAs share a head's K/V
+    const int i = blockIdx.x % p.n_tiles;
+    const int bh = blockIdx.x / p.n_tiles;
+    const int b = bh / p.H, h = bh % p.H, hk = h / p.G;
+    const int r0 = i * kTileM;
+    int jlo = 0, jhi = 0;
+    if (r0 < p.g.N) kv_tile_range(p.g, r0, r0 + kTileM < p.g.N ? r0 + kTileM : p.g.N, jlo, jhi);
+    const int n_items = jhi - jlo;
+
+    if (threadIdx.x == 0) init_ctl(sh, 1);
+    if (warp == kWarpMmaB) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
+
+    if (warp == kWarpTmaB && lane == 0 && n_items > 0) {
+        // ------------------------------------------------------------ TMA
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        const uint32_t fixed = smem_u32(&sh->fixed_full);
+        mbar_arrive_expect_tx(fixed, 2 * C::kTileBytes);
+        load_tile<D>(sQ, &p.tm_q, fixed, p.layout, b, h, r0);
+        load_tile<D>(sDO, &p.tm_do, fixed, p.layout, b, h, r0);
+        bool ok = true;
+        int n = 0;
+        for (; n < n_items && ok; ++n) {
+            const int st = n % C::kStages;
+            if (n >= C::kStages && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((n / C::kStages) - 1) & 1))) break;
+            const uint32_t full = smem_u32(&sh->ring_full[st]);
+            const uint32_t stage = sRing + st * C::kStageQ;
+            mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
+            load_tile<D>(stage, &p.tm_k, full, p.layout, b, hk, (jlo + n) * kTileN);
+            load_tile<D>(stage + C::kTileBytes, &p.tm_v, full, p.layout, b, hk, (jlo + n) * kTileN);
+        }
+        W.drain(fixed, 0);
+        for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
+            W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
+    } else if (warp == kWarpMmaB && lane == 0 && n_items > 0) {
+        // ------------------------------------------------------------ MMA
+        const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColA;
+        auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageQ; };
+        auto ring_full = [&](int n) { return W.wait(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
+        bool ok = W.wait(smem_u32(&sh->fixed_full), 0) && ring_full(0);
+        if (ok) {
+            tc_fence_after();
+            M::rows(tS, sQ, stage(0));                       // S = Q K^T
+            mma_commit(smem_u32(&sh->s_full));
+            M::rows(tDP, sDO, stage(0) + C::kTileBytes);     // dP = dO V^T
+            mma_commit(smem_u32(&sh->dp_full));
+        }
+        for (int n = 0; n < n_items && ok; ++n) {
+            if (n + 1 < n_items) {
+                // the next S may overwrite S once its row loads are done
+                if (!(ok = W.wait(smem_u32(&sh->s_free), n & 1) && ring_full(n + 1))) break;
+                tc_fence_after();
+                M::rows(tS, sQ, stage(n + 1));
+                mma_commit(smem_u32(&sh->s_full));
+            }
+            if (!(ok = W.wait(smem_u32(&sh->ds_full), n & 1))) break;
+            tc_fence_after();
+            M::cols(tDQ, tDP, stage(n), n > 0);               // dQ += dS K
+            mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
+            if (n + 1 < n_items) {
+                M::rows(tDP, sDO, stage(n + 1) + C::kTileBytes);
+                mma_commit(smem_u32(&sh->dp_full));
+            }
+        }
+        mma_commit(smem_u32(&sh->acc_done));
+        mma_commit(smem_u32(&sh->drain));
+        W.drain(smem_u32(&sh->drain), 0);
+    } else if (warp >= kWarpEw0) {
+        // ------------------------------------------------------- dS, epilogue
+        const int wq = warp - kWarpEw0;
+        const int row = wq * 32 + lane;
+        const int qi = r0 + row;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::kColS;
+        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        const size_t vrow = (size_t)bh * p.Npad + qi;
+        const float lse2 = p.lse2[vrow];
+        const float dsum = p.dsum[vrow];
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        for (int n = 0; n < n_items && ok; ++n) {
+            const int j = jlo + n;
+            if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
+            tc_fence_after();
+            uint32_t s[4][32];
+            ld_row128(tS, s);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh->s_free));
+            int c_lo = 0, c_hi = kTileN - 1;
+            if (tile_needs_mask(p.g, r0, j)) row_visible_cols(p.g, qi, j, c_lo, c_hi);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const int col = cc * 32 + v;
+                    const float e = ex2(fmaf(u2f(s[cc][v]), c2, -lse2));
+                    s[cc][v] = f2u(col < c_lo || col > c_hi ? 0.f : e);
+                }
+            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t d[32];
+                tmem_ld32(tDP + 32 * cc, d);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int v = 0; v < 16; ++v)
+                    pk[v] = pack2<kBf16>(u2f(s[cc][2 * v]) * (u2f(d[2 * v]) - dsum),
+                                         u2f(s[cc][2 * v + 1]) * (u2f(d[2 * v + 1]) - dsum));
+                tmem_st16(tDP + 16 * cc, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh->ds_full));
+        }
+        const bool live = qi < p.g.N;
+        const size_t orow = (size_t)row_index(p.layout, b, h, live ? qi : 0, p.H, p.g.N);
+        if (n_items == 0) {
+            if (live) zero_row<D>(p.dq, orow);
+        } else if (ok && W.wait_warp(smem_u32(&sh->acc_done), 0)) {
+            tc_fence_after();
+            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dq, orow, p.scale, live);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMmaB) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ===================================================================== pre
+// Dsum = rowsum(dO * O) and LSE * log2(e) per row, one warp per row, rows
+// past N (up to the padded length) filled so they contribute nothing.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* o, const uint16_t* d_o, const float* lse,
+                                                         float* lse2, float* dsum, int B, int H, int N, int Npad,
+                                                         int D, int layout) {
+    const long long rows = (long long)B * H * Npad;
+    const int lane = threadIdx.x & 31;
+    for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += ((long long)gridDim.x * blockDim.x) >> 5) {
+        const int i = (int)(r % Npad);
+        const long long bh = r / Npad;
+        float acc = 0.f;
+        float l2 = INFINITY;
+        if (i < N) {
+            const size_t base = (size_t)row_index(layout, (int)(bh / H), (int)(bh % H), i, H, N) * D;
+            for (int e = 2 * lane; e < D; e += 64) {
+                const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base + e);
+                const uint32_t g = *reinterpret_cast<const uint32_t*>(d_o + base + e);
+                acc = fmaf(lo_half<kBf16>(a), lo_half<kBf16>(g), acc);
+                acc = fmaf(hi_half<kBf16>(a), hi_half<kBf16>(g), acc);
+            }
+            const float l = lse[bh * N + i];
+            l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            lse2[bh * Npad + i] = l2;
+            dsum[bh * Npad + i] = acc;
+        }
+    }
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_bwd_typed(const BwdParams& p, int B, cudaStream_t s) {
+    auto kdkdv = fa_bwd_dkdv_kernel<D, kBf16>;
+    auto kdq = fa_bwd_dq_kernel<D, kBf16>;
+    constexpr int sm1 = dkdv_smem_bytes<D>();
+    constexpr int sm2 = dq_smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2);
+    if (e != cudaSuccess) return e;
+    kdkdv<<<B * p.Hkv * p.n_tiles, kBwdThreads, sm1, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kdq<<<B * p.H * p.n_tiles, kBwdThreads, sm2, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B, int H,
+                           int N, int Npad, int D, int layout, int dtype_code, int sms, cudaStream_t s) {
+    const long long rows = (long long)B * H * Npad;
+    long long grid = (rows * 32 + 255) / 256;
+    if (grid > 16LL * sms) grid = 16LL * sms;
+    if (dtype_code == 1)
+        fa_bwd_pre_kernel<true><<<(int)grid, 256, 0, s>>>(static_cast<const uint16_t*>(o),
+                                                            static_cast<const uint16_t*>(d_o), lse, lse2, dsum, B, H,
+                                                            N, Npad, D, layout);
+    else
+        fa_bwd_pre_kernel<false><<<(int)grid, 256, 0, s>>>(static_cast<const uint16_t*>(o),
+                                                             static_cast<const uint16_t*>(d_o), lse, lse2, dsum, B, H,
+                                                             N, Npad, D, layout);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int B, int D, bool bf16, cudaStream_t s) {
+    if (D == 64) return bf16 ? launch_bwd_typed<64, true>(p, B, s) : launch_bwd_typed<64, false>(p, B, s);
+    return bf16 ? launch_bwd_typed<128, true>(p, B, s) : launch_bwd_typed<128, false>(p, B, s);
+}
+
+}  // namespace fa

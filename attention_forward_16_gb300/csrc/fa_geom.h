@@ -66,6 +66,40 @@ FA_HD void row_visible_cols(const Geom& g, int i, int j, int& c_lo, int& c_hi) {
     c_hi = (int)(hi < -1 ? -1 : hi);
 }
 
+// Query-tile range [lo, hi) holding a row that sees some key of key tile j
+// (the transpose of kv_tile_range, for passes that hold a key tile and walk
+// the query tiles); lo == hi when no row sees any of its keys.
+FA_HD void q_tile_range(const Geom& g, int j, int& lo, int& hi) {
+    const long long c0 = (long long)j * kTileN;
+    long long c1 = c0 + kTileN - 1;
+    if (c1 > g.N - 1) c1 = g.N - 1;
+    long long rmin = g.win_r < 0 ? 0 : c0 - g.win_r;
+    long long rmax = g.win_l < 0 ? (long long)g.N - 1 : c1 + g.win_l;
+    if (rmin < 0) rmin = 0;
+    if (rmax > g.N - 1) rmax = g.N - 1;
+    if (c0 > g.N - 1 || rmin > rmax) {
+        lo = hi = 0;
+        return;
+    }
+    lo = (int)(rmin / kTileM);
+    hi = (int)(rmax / kTileM) + 1;
+}
+
+// Visible row interval [r_lo, r_hi] (tile-local, may be empty) of key kc
+// inside query tile i: rows r with kc - win_r <= r <= kc + win_l, r < N.
+FA_HD void key_visible_rows(const Geom& g, int kc, int i, int& r_lo, int& r_hi) {
+    const long long r0 = (long long)i * kTileM;
+    long long lo = g.win_r < 0 ? 0 : (long long)kc - g.win_r - r0;
+    long long hi = g.win_l < 0 ? (long long)kTileM - 1 : (long long)kc + g.win_l - r0;
+    const long long tail = (long long)g.N - 1 - r0;
+    if (hi > tail) hi = tail;
+    if (kc > g.N - 1) hi = -1;
+    if (lo < 0) lo = 0;
+    if (hi > kTileM - 1) hi = kTileM - 1;
+    r_lo = (int)(lo > kTileM ? kTileM : lo);
+    r_hi = (int)(hi < -1 ? -1 : hi);
+}
+
 // Fewest visible keys over rows [r0, r1) (r0 < r1 <= N).  The count per row,
 // min(N-1, i+win_r) - max(0, i-win_l) + 1, is concave in i, so the minimum
 // sits at one end of the range.

@@ -103,10 +103,58 @@ inline unsigned long long decode_workspace_bytes(long long BH, int Nq, int D, in
     return o_bytes + (rows * 4 + 255) / 256 * 256;
 }
 
+// Backward pass (dQ, dK, dV).  Rows are padded to a whole number of 128-row
+// tiles in the per-row vectors so the kernels copy them without tail checks.
+struct BwdParams {
+    CUtensorMap tm_q;   // 4-D maps as in TcParams: Q and dO with H heads,
+    CUtensorMap tm_k;   // K and V with H_kv heads
+    CUtensorMap tm_v;
+    CUtensorMap tm_do;
+    void* dq;           // Q's shape and layout, input element type
+    void* dk;           // K's shape and layout
+    void* dv;
+    const float* lse2;  // [B*H, Npad]: LSE * log2(e); +inf where a row sees no key and on padding
+    const float* dsum;  // [B*H, Npad]: rowsum(dO * O); 0 on padding
+    Geom g;
+    int H;              // query heads
+    int G;              // query heads per K/V head
+    int Hkv;
+    int layout;
+    int Npad;           // rows rounded up to kTileM
+    int n_tiles;        // Npad / kTileM
+    float scale;
+    float scale_log2;
+    unsigned long long wait_limit_ns;
+    int* status;
+};
+
+// Rotary position embedding of Q and K (one pass in HBM before attention).
+enum RopeStyle { ROPE_HALF = 0, ROPE_INTERLEAVED = 1 };
+
+struct RopeParams {
+    const void* x[2];   // Q, K (null: that tensor is skipped)
+    void* y[2];         // rotated outputs (may equal x)
+    int n[2];           // rows per (b, h): Nq, Nk
+    int heads[2];       // H, H_kv
+    int pos0[2];        // position of row 0
+    const float* cos;   // [n_pos, D/2]
+    const float* sin;
+    int B;
+    int D;              // multiple of 16
+    int style;
+    int layout;
+};
+
 // Launchers (return the CUDA error of the launch, if any).
 cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s);
 cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s);
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B,
+                           int H, int N, int Npad, int D, int layout, int dtype_code, int sms, cudaStream_t s);
+cudaError_t launch_bwd(const BwdParams& p, int B, int D, bool bf16, cudaStream_t s);
+cudaError_t launch_rope(const RopeParams& p, int dtype_code, int sms, cudaStream_t s);
+cudaError_t launch_rope_tables(float* cos_tab, float* sin_tab, int n_pos, int D, double base, int sms,
+                               cudaStream_t s);
 cudaError_t launch_selftest_timeout(int* status, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace fa

@@ -44,3 +44,12 @@ def algorithmic_bytes(B, H, N, D, dtype, o_dtype=None, with_lse=True):
     e = _ELEM[dtype]
     eo = _ELEM[o_dtype or dtype]
     return B * H * N * D * (3 * e + eo) + (B * H * N * 4 if with_lse else 0)
+
+
+def rope_bytes(w):
+    """Compulsory bytes of the rotary embedding pass of workload ``w``: Q and
+    K read and their rotated copies written, plus the cos/sin table read
+    once."""
+    esize = {"f16": 2, "bf16": 2, "f32": 4}[w.dtype]
+    qk = 2 * w.B * w.H * w.N * w.D * esize
+    return 2 * qk + 2 * w.N * (w.D // 2) * 4

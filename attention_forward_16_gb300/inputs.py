@@ -43,6 +43,8 @@ class Workload:
     win_r: int = -1
     input_scale: float = 1.0
     seed: int = 0
+    rope: str = ""            # "" (none), "half" or "interleaved": rotary embedding of Q and K first
+    rope_base: float = 10000.0
     notes: str = field(default="", compare=False)
 
 
@@ -56,6 +58,12 @@ WORKLOADS = {
     "bf16_full_4k": Workload("bf16_full_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128), MASK_NONE, seed=1003),
     "bf16_window_16k": Workload("bf16_window_16k", 1, 64, 16384, 128, "bf16", 1.0 / math.sqrt(128),
                                 MASK_WINDOW, 1024, 0, input_scale=0.5, seed=1005),
+    # the benchmark shape with the rotary embedding of Q and K in the step
+    "f16_rope_full_4k": Workload("f16_rope_full_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128), MASK_NONE,
+                                 seed=1003, rope="half", rope_base=10000.0),
+    # causal with the 500000 rotary base of the Llama-3 models the pages run
+    "bf16_rope_causal_4k": Workload("bf16_rope_causal_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128),
+                                    MASK_CAUSAL, seed=1004, rope="half", rope_base=500000.0),
 }
 
 

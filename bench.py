@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused attention fwd TFLOP/s and % of GB300 dense FP16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0   # only if the measured-peaks file is absent
+FALLBACK_HBM_GBS = 6800.0
 
 
 def _env_int(name, default):
@@ -64,13 +65,18 @@ def measured_peaks():
     if os.path.exists(path):
         with open(path) as f:
             return json.load(f), "measured"
-    return {"bf16_tflops": FALLBACK_PEAK_TFLOPS}, "fallback"
+    return {"bf16_tflops": FALLBACK_PEAK_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def kernel_source_hash():
+# Sources the tensor-core forward kernel is compiled from (its own file and
+# the headers it includes): a recorded traffic figure holds while they do.
+FWD_KERNEL_SOURCES = ("fa_tc.cu", "tc_common.cuh", "ptx.cuh", "fa_geom.h", "fa_internal.h")
+
+
+def kernel_source_hash(files=FWD_KERNEL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_forward_16_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -182,20 +188,32 @@ def cpu_oracle_sample(w, q, k, v, budget_s, rows=None):
     from attention_forward_16_gb300.flops import visible_keys_per_row
     qd, kd, vd = (t.float().numpy() for t in (q, k, v))
     per_row = visible_keys_per_row(w.N, w.mask, w.win_l, w.win_r)
+    rot = oracle_rotation(w)
     done_flops, heads, t_total = 0, 0, 0.0
     r = rows or w.N
     while t_total < budget_s and heads < w.B * w.H:
         b, h = divmod(heads, w.H)
         r0 = (heads * 977) % max(1, w.N - r + 1) if rows else 0
         t0 = time.perf_counter()
-        attention_three_pass(qd[b:b + 1, h:h + 1, r0:r0 + r], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
-                             w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
+        attention_three_pass(rot(qd[b:b + 1, h:h + 1, r0:r0 + r], r0), rot(kd[b:b + 1, h:h + 1], 0),
+                             vd[b:b + 1, h:h + 1], w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
         t_total += time.perf_counter() - t0
         done_flops += 4 * w.D * int(per_row[r0:r0 + r].sum())
         heads += 1
     desc = f"{heads} of {w.B * w.H} heads" + (f", {r} query rows each" if rows else ", all rows") + \
-        f" of {w.name}, float64 numpy, {t_total:.1f} s"
+        f" of {w.name}, float64 numpy" + (", rotary embedding of the head's Q rows and K" if w.rope else "") + \
+        f", {t_total:.1f} s"
     return done_flops / t_total / 1e12, desc, blas_threads()
+
+
+def oracle_rotation(w):
+    """x, pos0 -> the oracle's rotary embedding of x (identity without rope)."""
+    if not w.rope:
+        return lambda x, pos0: x
+    from oracle import STYLE_HALF, STYLE_INTERLEAVED, apply_rope, rope_tables
+    cos, sin = rope_tables(w.N, w.D, w.rope_base)
+    style = STYLE_HALF if w.rope == "half" else STYLE_INTERLEAVED
+    return lambda x, pos0: apply_rope(x, cos, sin, style, pos0)
 
 
 def blas_threads():
@@ -223,12 +241,13 @@ def run_reference(args, w, world, rank):
     per_row = visible_keys_per_row(w.N, w.mask, w.win_l, w.win_r)
     qd, kd, vd = (t.float().numpy() for t in (q, k, v))
     rows = 64
+    rot = oracle_rotation(w)
 
     def step(i):
         b, h = divmod(i % (w.B * w.H), w.H)
         r0 = (i * 977) % (w.N - rows + 1)
-        attention_three_pass(qd[b:b + 1, h:h + 1, r0:r0 + rows], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
-                             w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
+        attention_three_pass(rot(qd[b:b + 1, h:h + 1, r0:r0 + rows], r0), rot(kd[b:b + 1, h:h + 1], 0),
+                             vd[b:b + 1, h:h + 1], w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
         return 4 * w.D * int(per_row[r0:r0 + rows].sum())
 
     for i in range(args.warmup):
@@ -244,7 +263,8 @@ def run_reference(args, w, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype_in": w.dtype,
-                   "mask": w.mask, "window": [w.win_l, w.win_r], "step": f"{rows} query rows of one head"},
+                   "mask": w.mask, "window": [w.win_l, w.win_r], "rope": w.rope or None,
+                   "step": f"{rows} query rows of one head"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": f"{rows} query rows x full keys of one (b, h) per step, float64 numpy"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -260,7 +280,7 @@ def run_native(args, w, world, rank, local, pg):
     import torch
     import attention_forward_16_gb300 as fa
     from attention_forward_16_gb300.build import build
-    from attention_forward_16_gb300.flops import algorithmic_bytes, attention_flops
+    from attention_forward_16_gb300.flops import algorithmic_bytes, attention_flops, rope_bytes
     from attention_forward_16_gb300.inputs import make_workload
 
     build()
@@ -274,9 +294,24 @@ def run_native(args, w, world, rank, local, pg):
     window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
     causal = w.mask == fa.FA_MASK_CAUSAL
     stream = torch.cuda.current_stream(device)
+    rope = bool(w.rope)
+    if rope:
+        # the cos/sin table is an input the caller owns, built once
+        cos, sin = fa.rope_tables(w.N, w.D, w.rope_base, device=device)
+        rq, rk = torch.empty_like(dq), torch.empty_like(dk)
+
+    def rotate(sq, sk, oq, ok_, s_=None):
+        fa.apply_rope(sq, sk, cos, sin, style=w.rope, q_out=oq, k_out=ok_, stream=s_)
+
+    def attend(aq, ak, av, ao, al, s_=None):
+        fa.attention_fwd(aq, ak, av, scale=w.scale, causal=causal, window=window, out=ao, lse=al, stream=s_)
 
     def step():
-        fa.attention_fwd(dq, dk, dv, scale=w.scale, causal=causal, window=window, out=do, lse=dl)
+        if rope:
+            rotate(dq, dk, rq, rk)
+            attend(rq, rk, dv, do, dl)
+        else:
+            attend(dq, dk, dv, do, dl)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -286,15 +321,27 @@ def run_native(args, w, world, rank, local, pg):
 
     clocks = ClockSampler(local).start() if rank == 0 else None
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if rope else 0)]
     barrier(pg, device)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+        # the attention launch is bracketed alone (the roofline's kernel); the
+        # rotation, when the workload has one, gets its own pair of events
+        if rope:
+            rev[i][0].record(stream)
+            rotate(dq, dk, rq, rk)
+            rev[i][1].record(stream)
+            ev[i][0].record(stream)
+            attend(rq, rk, dv, do, dl)
+            ev[i][1].record(stream)
+        else:
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(pg, device)
@@ -305,6 +352,7 @@ def run_native(args, w, world, rank, local, pg):
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = reduce_max(pg, total_ms, device)
     avg_launch_ms = reduce_max(pg, sum(launch_ms) / len(launch_ms), device)
+    rope_ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in rev) / len(rev), device) if rope else None
 
     flops_step = attention_flops(w.B, w.H, w.N, w.D, w.mask, w.win_l, w.win_r)
     value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
@@ -317,6 +365,7 @@ def run_native(args, w, world, rank, local, pg):
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
     bufs = [(dq, dk, dv, do, dl)] + [tuple(torch.empty_like(t) for t in (dq, dk, dv, do, dl))]
+    rbufs = [(rq, rk), (torch.empty_like(dq), torch.empty_like(dk))] if rope else None
     houts = [(torch.empty(do.shape, dtype=do.dtype, pin_memory=True),
               torch.empty(dl.shape, dtype=dl.dtype, pin_memory=True)) for _ in range(2)]
 
@@ -328,7 +377,12 @@ def run_native(args, w, world, rank, local, pg):
             bq.copy_(hq, non_blocking=True)
             bk.copy_(hk, non_blocking=True)
             bv.copy_(hv, non_blocking=True)
-            fa.attention_fwd(bq, bk, bv, scale=w.scale, causal=causal, window=window, out=bo, lse=bl, stream=s_)
+            if rope:
+                xq, xk = rbufs[i % 2]
+                rotate(bq, bk, xq, xk, s_)
+                attend(xq, xk, bv, bo, bl, s_)
+            else:
+                attend(bq, bk, bv, bo, bl, s_)
             ho.copy_(bo, non_blocking=True)
             hl.copy_(bl, non_blocking=True)
 
@@ -378,10 +432,21 @@ def run_native(args, w, world, rank, local, pg):
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
-                "how": "attention_fwd on host inputs: pinned H2D copy, fused forward, D2H of O and LSE every step; "
+                "how": "attention_fwd on host inputs: pinned H2D copy, " + ("rotary embedding, " if rope else "") +
+                       "fused forward, D2H of O and LSE every step; "
                        "steps alternate over two streams so copies overlap the previous step's kernel"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if rope else 1),
     }
+    if rope:
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        rb = rope_bytes(w)
+        line["config"]["rope"] = {"style": w.rope, "base": w.rope_base}
+        line["rope_kernel"] = {
+            "kernel": "fa_rope_kernel<%s,%s>" % (w.dtype, w.rope), "avg_launch_ms": rope_ms,
+            "share_of_step": rope_ms / (total_ms / args.steps),
+            "roofline": {"bound": "hbm", "achieved": rb / (rope_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": rb / (rope_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": rb,
+                         "peak_source": peak_src}}
     if world == 1 and not args.no_cpu_baseline:
         tf, desc, cores = cpu_oracle_sample(w, q, k, v, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
@@ -434,7 +499,7 @@ def run_decode(args, w, world, rank, local, pg):
     if rank != 0:
         return 0
     peaks, src = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     gbs = nbytes / (ms / 1e3) / 1e9
     line = {
         "metric": "attention decode HBM GB/s (split-K, K/V cache read once)", "value": gbs * world, "unit": "GB/s",

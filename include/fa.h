@@ -227,6 +227,91 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
                void* stream);
 
 /*
+ * fa_bwd -- gradients dQ, dK, dV of the attention above for an upstream
+ * gradient dO of O.  The ops-transformer walk-through's closing remarks say
+ * the operator also has a backward pass, without writing it out; this is the
+ * chain rule through the definition of "Ascend C advanced practice:
+ * high-performance FlashAttention-2-style tile-level fused attention",
+ * section 1.1, with P recomputed from the forward's LSE:
+ *     P = exp(scale * Q K^T + mask - LSE)      Dsum_i = sum_d dO_id O_id
+ *     dV = P^T dO     dS = P * (dO V^T - Dsum)
+ *     dQ = scale * dS K      dK = scale * dS^T Q
+ * Grouped K/V heads (H_kv < H) sum the gradients of the query heads that
+ * share a K/V head.  The LSE output itself is not differentiated.
+ *
+ * q, o, d_o, dq: [B, H, N, D] (or [B, N, H, D] for FA_LAYOUT_BNHD); k, v,
+ * dk, dv: [B, H_kv, N, D] / [B, N, H_kv, D]; lse: [B, H, N] fp32 as fa_fwd_gqa
+ * returned it.  dtype FA_F16 or FA_BF16 for every tensor (O as the forward
+ * wrote it in that type); D = 64 or 128.  P and dS enter the tensor-core
+ * products rounded to dtype; everything else is fp32.  The three outputs are
+ * written in full (rows no query sees get zeros) and must not overlap any
+ * input.  `workspace` is caller-owned device memory of at least
+ * fa_bwd_workspace_bytes(B, H, N) bytes, 256-byte aligned, used by this call
+ * only; other pointers 16-byte aligned (lse 4).
+ *
+ * Returns FA_OK (enqueued on `stream`), FA_ERR_ARG (bad size, mask, H_kv,
+ * layout, scale, a NULL pointer, a small workspace), FA_ERR_UNSUPPORTED
+ * (FA_F32 or another D), FA_ERR_ALIGN or FA_ERR_CUDA; kernel wait timeouts
+ * are reported by fa_device_status().
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D, float scale,
+           int mask_kind, int win_l, int win_r, int dtype, int layout,
+           void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/* Workspace fa_bwd needs for B x H rows of length N (two fp32 values per row,
+ * rows padded to a multiple of 128).  FA_OK or FA_ERR_ARG. */
+int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes);
+
+/* Pairings of the rotary embedding (fa_rope). */
+enum {
+    FA_ROPE_HALF = 0,        /* pair i is (i, i + D/2): rotate-half form     */
+    FA_ROPE_INTERLEAVED = 1  /* pair i is (2i, 2i + 1)                       */
+};
+
+/*
+ * fa_rope -- rotary position embedding of Q and/or K, run before fa_fwd_gqa
+ * or fa_decode_gqa.  "Ascend C advanced practice: high-performance
+ * FlashAttention-2-style tile-level fused attention", section 9 ("Extensions:
+ * integration with RoPE and a paged KV cache"), rotates the Q and K blocks as
+ * they are loaded, using a cos/sin table.  The page gives no formula; this is
+ * the standard rotary embedding.  Row n of Q sits at position p = q_pos0 + n
+ * (of K: k_pos0 + n), and each of its D/2 pairs (x_a, x_b), pair i, becomes
+ *     x_a' = x_a cos_tab[p][i] - x_b sin_tab[p][i]
+ *     x_b' = x_b cos_tab[p][i] + x_a sin_tab[p][i]
+ * in fp32, rounded once to the element type.  Here it is one streaming pass
+ * over Q and K in device memory rather than a step inside the attention
+ * kernel's tile loads: each K tile is loaded by every CTA of its head, so a
+ * rotation there would be repeated N/256 times per head and would compete for
+ * the shared-memory bandwidth the tensor-core products need.
+ *
+ * q, q_out: [B, H, Nq, D] (FA_LAYOUT_BHND) or [B, Nq, H, D] (FA_LAYOUT_BNHD).
+ * k, k_out: [B, H_kv, Nk, D] or [B, Nk, H_kv, D].  dtype: FA_F16, FA_BF16 or
+ * FA_F32 for all four.  cos_tab, sin_tab: fp32 [n_pos, D/2] row-major
+ * (fa_rope_tables fills them).  Either q or k may be NULL to skip that tensor
+ * (its out pointer must then be NULL as well; its sizes are ignored).  In
+ * place is allowed (q_out == q, k_out == k); any other overlap is not.  All
+ * pointers are caller-owned device memory, 16-byte aligned.
+ *
+ * Returns FA_OK (enqueued on `stream`), FA_ERR_ARG (a size <= 0, D not a
+ * multiple of 16 or above 1024, a position outside [0, n_pos), bad style or
+ * layout, missing pointers), FA_ERR_UNSUPPORTED (dtype), FA_ERR_ALIGN or
+ * FA_ERR_CUDA.
+ */
+int fa_rope(const void* q, const void* k, void* q_out, void* k_out, const float* cos_tab, const float* sin_tab,
+            int B, int H, int H_kv, int Nq, int Nk, int D, int q_pos0, int k_pos0, int n_pos,
+            int style, int dtype, int layout, void* stream);
+
+/*
+ * fa_rope_tables -- fill cos_tab and sin_tab (fp32 [n_pos, D/2], caller-owned
+ * device memory, 16-byte aligned) with cos and sin of p * base^(-2i/D) for
+ * position p and pair i, each computed in double precision and rounded once.
+ * Returns FA_OK, FA_ERR_ARG (n_pos <= 0, D odd, <= 0 or above 1024, base not
+ * a positive finite number, NULL table), FA_ERR_ALIGN or FA_ERR_CUDA.
+ */
+int fa_rope_tables(float* cos_tab, float* sin_tab, int n_pos, int D, double base, void* stream);
+
+/*
  * fa_device_status -- synchronise `stream`, then report and clear the
  * library's device status word.  Returns FA_OK, FA_ERR_TIMEOUT (a kernel
  * wait ran past its limit; the kernel stopped early and its outputs are

@@ -1,0 +1,173 @@
+"""Rotary embedding on the GPU (fa_rope, fa_rope_tables) against the oracle.
+
+Bounds.  The kernel forms x_a c - x_b s in fp32 and rounds once to the
+element type, so each output lies within 4 * 2^-24 * (|x_a| + |x_b|) (the two
+products and the sum, |c|, |s| <= 1) plus half an ulp of the element type
+from the float64 result.  The table kernel rounds a double-precision cos/sin
+once to fp32: within 2^-25 for values below 1 in magnitude.  Attention on the
+rotated Q and K keeps the forward's bounds against the oracle on the same
+rotated, rounded inputs: O written in the 16-bit input type is off by up to
+half an ulp of |O| from that rounding alone, so |dO| minus half an ulp of the
+oracle value must stay <= 2e-3, and |dLSE| <= 1e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_16_gb300 as fa
+from attention_forward_16_gb300.inputs import make_qkv
+from oracle import (MASK_CAUSAL, MASK_NONE, STYLE_HALF, STYLE_INTERLEAVED, apply_rope, attention_grouped,
+                    attention_rope, rope_tables)
+
+pytestmark = pytest.mark.gpu
+
+_STYLE = {"half": STYLE_HALF, "interleaved": STYLE_INTERLEAVED}
+_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_forward_16_gb300.build import build
+    build()
+    fa.load()
+
+
+def _half_ulp(x, dtype):
+    if dtype == "f32":
+        return np.zeros_like(x)
+    mant = {"f16": 10, "bf16": 7}[dtype]
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    return 0.5 * np.exp2(np.floor(np.log2(ax)) - mant)
+
+
+def _partner(D, style):
+    i = np.arange(D)
+    return (i + D // 2) % D if style == "half" else i ^ 1
+
+
+def _check_rot(got, x, cos64, sin64, style, pos0, dtype, seq_axis, what):
+    ref = apply_rope(x, cos64, sin64, _STYLE[style], pos0, seq_axis=seq_axis)
+    D = x.shape[-1]
+    bound = 4 * 2.0 ** -24 * (np.abs(x) + np.abs(x[..., _partner(D, style)])) + _half_ulp(ref, dtype) * 1.0001
+    # a value that rounds up across a binade edge has the larger ulp
+    bound = np.maximum(bound, 4 * 2.0 ** -24 * (np.abs(x) + np.abs(x[..., _partner(D, style)])) +
+                       _half_ulp(got, dtype) * 1.0001)
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), f"{what}: worst excess {(err - bound).max():.3e}"
+
+
+def _host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def test_tables_match_oracle():
+    for n_pos, D, base in [(4096, 128, 10000.0), (33, 64, 500000.0), (7, 16, 10.0)]:
+        cos, sin = fa.rope_tables(n_pos, D, base)
+        torch.cuda.synchronize()
+        rc, rs = rope_tables(n_pos, D, base)
+        assert np.abs(_host(cos) - rc).max() <= 2.0 ** -25 + 1e-12
+        assert np.abs(_host(sin) - rs).max() <= 2.0 ** -25 + 1e-12
+
+
+def test_tables_far_positions():
+    cos, sin = fa.rope_tables(131072, 128, 500000.0)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 4095, 65537, 131071])
+    rc, rs = rope_tables(131072, 128, 500000.0)
+    assert np.abs(_host(cos)[rows] - rc[rows]).max() <= 2.0 ** -25 + 1e-12
+    assert np.abs(_host(sin)[rows] - rs[rows]).max() <= 2.0 ** -25 + 1e-12
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_rotation_matches_oracle(dtype, style, layout, D):
+    B, H, Hkv, Nq, Nk = 2, 4, 2, 37, 301
+    q, _, _ = make_qkv(B, H, Nq, D, dtype, seed=D + len(style), n_k=1)
+    _, k, _ = make_qkv(B, Hkv, 1, D, dtype, seed=D + 7, n_k=Nk)
+    n_pos = 400
+    cos, sin = fa.rope_tables(n_pos, D, 10000.0)
+    c64, s64 = _host(cos), _host(sin)
+    perm = (lambda t: t.permute(0, 2, 1, 3).contiguous()) if layout == "bnhd" else (lambda t: t)
+    seq_axis = -3 if layout == "bnhd" else -2
+    qd, kd = perm(q).cuda(), perm(k).cuda()
+    for qp, kp in [(0, 0), (50, 99)]:
+        qr, kr = fa.apply_rope(qd, kd, cos, sin, style=style, q_pos0=qp, k_pos0=kp, layout=layout)
+        torch.cuda.synchronize()
+        what = f"{dtype} {style} {layout} D={D} pos=({qp},{kp})"
+        _check_rot(_host(qr), _host(perm(q)), c64, s64, style, qp, dtype, seq_axis, "q " + what)
+        _check_rot(_host(kr), _host(perm(k)), c64, s64, style, kp, dtype, seq_axis, "k " + what)
+
+
+def test_in_place_equals_out_of_place_and_single_tensors():
+    q, k, _ = make_qkv(1, 3, 129, 128, "bf16", seed=11)
+    cos, sin = fa.rope_tables(200, 128)
+    qd, kd = q.cuda(), k.cuda()
+    qr, kr = fa.apply_rope(qd, kd, cos, sin, q_pos0=3, k_pos0=3)
+    q_only, none_k = fa.apply_rope(qd, None, cos, sin, q_pos0=3)
+    none_q, k_only = fa.apply_rope(None, kd, cos, sin, k_pos0=3)
+    qi, ki = qd.clone(), kd.clone()
+    fa.apply_rope(qi, ki, cos, sin, q_pos0=3, k_pos0=3, inplace=True)
+    torch.cuda.synchronize()
+    assert none_k is None and none_q is None
+    assert torch.equal(qr, q_only) and torch.equal(kr, k_only)
+    assert torch.equal(qr, qi) and torch.equal(kr, ki)
+
+
+def test_single_row_and_position_zero_is_identity():
+    q, _, _ = make_qkv(1, 1, 1, 64, "f16", seed=12)
+    cos, sin = fa.rope_tables(1, 64)
+    qr, _ = fa.apply_rope(q.cuda(), None, cos, sin)
+    torch.cuda.synchronize()
+    assert torch.equal(qr.cpu(), q)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("mk", [MASK_NONE, MASK_CAUSAL])
+def test_attention_with_rope_matches_oracle(dtype, mk):
+    B, H, Hkv, N, D = 1, 4, 2, 700, 128
+    q, _, _ = make_qkv(B, H, N, D, dtype, seed=13, n_k=1)
+    _, k, v = make_qkv(B, Hkv, 1, D, dtype, seed=14, n_k=N)
+    cos, sin = fa.rope_tables(N + 100, D, 500000.0)
+    c64, s64 = _host(cos), _host(sin)
+    o, lse = fa.attention_fwd_rope(q.cuda(), k.cuda(), v.cuda(), cos, sin, pos0=100, causal=mk == MASK_CAUSAL)
+    torch.cuda.synchronize()
+    o, lse = _host(o), lse.cpu().numpy().astype(np.float64)
+    scale = 1.0 / math.sqrt(D)
+    td = _TORCH[dtype]
+    # the same rotated inputs, rounded to the element type as the kernel stores them
+    qr = torch.from_numpy(apply_rope(q.double().numpy(), c64, s64, STYLE_HALF, 100)).to(td).double().numpy()
+    kr = torch.from_numpy(apply_rope(k.double().numpy(), c64, s64, STYLE_HALF, 100)).to(td).double().numpy()
+    ro, rl = attention_grouped(qr, kr, v.double().numpy(), scale, mk)
+    assert (np.abs(o - ro) - _half_ulp(ro, dtype)).max() <= 2e-3 and np.abs(lse - rl).max() <= 1e-3
+    if dtype == "f16":
+        # fp16's 2^-11 rounding of the stored rotated Q and K moves the scores
+        # little enough that the unrounded definition meets the same bound;
+        # bf16's 2^-8 does not, exactly as for any bf16 input (measured
+        # 2.1e-3), so bf16 is held to the rounded inputs above
+        ro2, rl2 = attention_rope(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale, c64, s64,
+                                  STYLE_HALF, mk, q_pos0=100, k_pos0=100)
+        assert (np.abs(o - ro2) - _half_ulp(ro2, dtype)).max() <= 2e-3 and np.abs(lse - rl2).max() <= 1e-3
+
+
+def test_full_size_rotation_sampled_rows():
+    """The benchmark shape, B=4 H=32 N=4096 D=128 fp16: 256 sampled rows."""
+    B, H, N, D = 4, 32, 4096, 128
+    q, k, _ = make_qkv(B, H, N, D, "f16", seed=15)
+    cos, sin = fa.rope_tables(N, D, 10000.0)
+    qr, kr = fa.apply_rope(q.cuda(), k.cuda(), cos, sin)
+    torch.cuda.synchronize()
+    c64, s64 = _host(cos), _host(sin)
+    rng = np.random.default_rng(16)
+    for src, out in ((q, qr), (k, kr)):
+        for _ in range(128):
+            b, h, n = int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))
+            x = src[b, h, n:n + 1].double().numpy()[None, None]
+            got = out[b, h, n:n + 1].float().cpu().double().numpy()[None, None]
+            _check_rot(got, x, c64, s64, "half", n, "f16", -2, f"row ({b},{h},{n})")

@@ -204,3 +204,47 @@ def _plan(BH, Nk, sms, req):
     c = -(-Nk // s)
     c = -(-c // 4) * 4
     return -(-Nk // c), c
+
+
+# --------------------------------------------------------- RoPE: host checks
+
+def _rope(lib, q=16, k=32, qo=48, ko=64, cos=80, sin=96, B=1, H=2, Hkv=1, Nq=4, Nk=4, D=64, qp=0, kp=0, n_pos=8,
+          st=0, dt=0, lay=0):
+    return lib.fa_rope(q, k, qo, ko, cos, sin, B, H, Hkv, Nq, Nk, D, qp, kp, n_pos, st, dt, lay, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None, k=None, qo=None, ko=None), fb.FA_ERR_ARG),
+    (dict(q=None), fb.FA_ERR_ARG),              # out given without its input
+    (dict(ko=None), fb.FA_ERR_ARG),
+    (dict(cos=None), fb.FA_ERR_ARG),
+    (dict(B=0), fb.FA_ERR_ARG),
+    (dict(D=40), fb.FA_ERR_ARG),                 # not a multiple of 16
+    (dict(D=2048), fb.FA_ERR_ARG),
+    (dict(st=2), fb.FA_ERR_ARG),
+    (dict(lay=3), fb.FA_ERR_ARG),
+    (dict(qp=5), fb.FA_ERR_ARG),                 # rows 5..8 leave an 8-row table
+    (dict(kp=-1), fb.FA_ERR_ARG),
+    (dict(Nk=9), fb.FA_ERR_ARG),
+    (dict(Hkv=0), fb.FA_ERR_ARG),
+    (dict(dt=3), fb.FA_ERR_UNSUPPORTED),
+    (dict(q=24), fb.FA_ERR_ALIGN),
+    (dict(ko=8), fb.FA_ERR_ALIGN),
+    (dict(sin=100), fb.FA_ERR_ALIGN),
+])
+def test_rope_validation_rejects_before_any_launch(lib, kw, code):
+    assert _rope(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_pos=0), fb.FA_ERR_ARG),
+    (dict(D=7), fb.FA_ERR_ARG),
+    (dict(base=0.0), fb.FA_ERR_ARG),
+    (dict(base=float("inf")), fb.FA_ERR_ARG),
+    (dict(cos=None), fb.FA_ERR_ARG),
+    (dict(cos=20), fb.FA_ERR_ALIGN),
+])
+def test_rope_tables_validation(lib, kw, code):
+    a = dict(cos=16, sin=32, n_pos=4, D=8, base=10000.0)
+    a.update(kw)
+    assert lib.fa_rope_tables(a["cos"], a["sin"], a["n_pos"], a["D"], a["base"], None) == code
