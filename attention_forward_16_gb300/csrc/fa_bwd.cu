@@ -21,11 +21,17 @@
 // atomics from the dkdv kernel: two more products per tile pair, in exchange
 // for a deterministic result and no read-modify-write traffic in L2.
 //
-// Warp roles in both kernels (256 threads): warp 0 issues TMA loads, warp 1
-// allocates TMEM and one of its threads issues tcgen05.mma, warps 4-7 turn
-// scores into P and dS (one TMEM lane = one row per thread) and write the
-// result; warps 2-3 only take part in the CTA barriers.  Every mbarrier
-// wait is bounded, as in the forward kernel.
+// Warp roles in both kernels (384 threads): warp 0 issues TMA loads, warp 1
+// allocates TMEM and one of its threads issues tcgen05.mma, warps 4-11 turn
+// scores into P and dS and write the result; warps 2-3 only take part in the
+// CTA barriers.  Warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (one
+// row per thread) and split the 128 columns of a tile: nothing in P or dS
+// reduces over a row, so the halves never exchange values, and two warps per
+// sub-partition hide the exponential's latency better than one.  Each half
+// writes its 16-bit P or dS into the first columns of its own fp32 half, so
+// neither overwrites values the other still reads; the products that read
+// them from TMEM address the halves separately.  Every mbarrier wait is
+// bounded, as in the forward kernel.
 #include <cmath>
 
 #include "fa_internal.h"
@@ -35,10 +41,11 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
 constexpr int kWarpTmaB = 0;
 constexpr int kWarpMmaB = 1;
-constexpr int kWarpEw0 = 4;  // first of the four elementwise warps
+constexpr int kWarpEw0 = 4;  // first of the eight elementwise warps (4 .. 11)
+constexpr int kEwThreads = 256;
 constexpr float kLog2e = 1.4426950408889634074f;
 
 template <int D>
@@ -107,12 +114,13 @@ struct Mma {
             mma_ss(dst, make_sdesc(a + off, 16, 1024), make_sdesc(b + off, 16, 1024), kIdescRows, kk > 0);
         }
     }
-    // dst[128 x D] (+)= T[128 x 128] (16-bit, TMEM columns at `t`) B[128 x D].
+    // dst[128 x D] (+)= T[128 x 128] B[128 x D]: T 16-bit in TMEM, its K
+    // columns [64 h, 64 h + 64) packed at TMEM column t + 64 h (32 columns).
     static __device__ __forceinline__ void cols(uint32_t dst, uint32_t t, uint32_t b, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
             const uint64_t bd = make_sdesc(b + kk * 2048, BwdCfg<D>::kBoxBytes, 1024);
-            mma_ts(dst, t + kk * 8, bd, kIdescCols, (acc || kk > 0) ? 1u : 0u);
+            mma_ts(dst, t + (kk / 4) * 64 + (kk % 4) * 8, bd, kIdescCols, (acc || kk > 0) ? 1u : 0u);
         }
     }
 };
@@ -124,10 +132,10 @@ __device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count) {
         mbar_init(smem_u32(&sh->ring_empty[s]), ring_empty_count);
     }
     mbar_init(smem_u32(&sh->s_full), 1);
-    mbar_init(smem_u32(&sh->s_free), 128);
+    mbar_init(smem_u32(&sh->s_free), kEwThreads);
     mbar_init(smem_u32(&sh->dp_full), 1);
-    mbar_init(smem_u32(&sh->p_full), 128);
-    mbar_init(smem_u32(&sh->ds_full), 128);
+    mbar_init(smem_u32(&sh->p_full), kEwThreads);
+    mbar_init(smem_u32(&sh->ds_full), kEwThreads);
     mbar_init(smem_u32(&sh->acc_done), 1);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
@@ -135,18 +143,19 @@ __device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count) {
     fence_proxy_async_smem();
 }
 
-// One 128-column row of fp32 values from TMEM into registers.
-__device__ __forceinline__ void ld_row128(uint32_t t, uint32_t (&r)[4][32]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(t + c * 32, r[c]);
+// A thread's 64-column half row of fp32 values from TMEM into registers.
+__device__ __forceinline__ void ld_half(uint32_t t, uint32_t (&r)[2][32]) {
+    tmem_ld32(t, r[0]);
+    tmem_ld32(t + 32, r[1]);
     tmem_wait_ld();
 }
 
-// Store a thread's row of a 16-bit gradient (fp32 in TMEM, times `mul`).
+// Store half `hf` of the columns of a thread's row of a 16-bit gradient
+// (fp32 in TMEM, times `mul`).
 template <int D, bool kBf16>
-__device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, float mul, bool live) {
+__device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, int hf, float mul, bool live) {
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
         uint32_t v[32];
         tmem_ld32(t + c * 32, v);
         tmem_wait_ld();
@@ -163,10 +172,10 @@ __device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, flo
 }
 
 template <int D>
-__device__ __forceinline__ void zero_row(void* out, size_t row) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D);
+__device__ __forceinline__ void zero_row(void* out, size_t row, int hf) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D + hf * (D / 2));
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
 // ===================================================================== dK, dV
@@ -274,35 +283,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
         W.drain(smem_u32(&sh->drain), 0);
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------- P, dS, epilogue
-        const int wq = warp - kWarpEw0;
-        const int c = wq * 32 + lane;          // key row within the tile
+        const int wq = (warp - kWarpEw0) & 3;   // TMEM lane quarter
+        const int hf = (warp - kWarpEw0) >> 2;  // query-column half of the tile
+        const int c = wq * 32 + lane;           // key row within the tile
         const int kc = j * kTileN + c;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS;
-        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        const uint32_t tS = tmem + lane_base + C::kColS + hf * 64;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * 64;
         const float c2 = p.scale_log2;
         bool ok = true;
         for (int n = 0; n < n_items && ok; ++n) {
             int h, i;
             item(n, h, i);
             const uint8_t* stage = smem + 2 * C::kTileBytes + (n % C::kStages) * C::kStageKV;
-            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes);
-            const float4* dsum = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes);
+            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes) + hf * 16;
+            const float4* dsum = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * 16;
             if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1))) break;
             if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
             tc_fence_after();
-            uint32_t s[4][32];
-            ld_row128(tS, s);
+            uint32_t s[2][32];
+            ld_half(tS, s);
             int r_lo = 0, r_hi = kTileM - 1;
             if (tile_needs_mask(p.g, i * kTileM, j)) key_visible_rows(p.g, kc, i, r_lo, r_hi);
-            // P^T row: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
+            // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const float4 l4 = lse2[cc * 8 + v];
-                    const int q = cc * 32 + 4 * v;
+                    const int q = hf * 64 + cc * 32 + 4 * v;
                     float e0 = ex2(fmaf(u2f(s[cc][4 * v]), c2, -l4.x));
                     float e1 = ex2(fmaf(u2f(s[cc][4 * v + 1]), c2, -l4.y));
                     float e2 = ex2(fmaf(u2f(s[cc][4 * v + 2]), c2, -l4.z));
@@ -323,22 +333,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->p_full));
-            // dS^T row: p * (dP - Dsum_q), written over the dP columns already read
+            // dS^T: p * (dP - Dsum_q), written over dP columns of this half already read
             if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
             tc_fence_after();
+            uint32_t d[2][32];
+            ld_half(tDP, d);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t d[32];
-                tmem_ld32(tDP + 32 * cc, d);
-                tmem_wait_ld();
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const float4 d4 = dsum[cc * 8 + v];
-                    const float g0 = u2f(s[cc][4 * v]) * (u2f(d[4 * v]) - d4.x);
-                    const float g1 = u2f(s[cc][4 * v + 1]) * (u2f(d[4 * v + 1]) - d4.y);
-                    const float g2 = u2f(s[cc][4 * v + 2]) * (u2f(d[4 * v + 2]) - d4.z);
-                    const float g3 = u2f(s[cc][4 * v + 3]) * (u2f(d[4 * v + 3]) - d4.w);
+                    const float g0 = u2f(s[cc][4 * v]) * (u2f(d[cc][4 * v]) - d4.x);
+                    const float g1 = u2f(s[cc][4 * v + 1]) * (u2f(d[cc][4 * v + 1]) - d4.y);
+                    const float g2 = u2f(s[cc][4 * v + 2]) * (u2f(d[cc][4 * v + 2]) - d4.z);
+                    const float g3 = u2f(s[cc][4 * v + 3]) * (u2f(d[cc][4 * v + 3]) - d4.w);
                     pk[2 * v] = pack2<kBf16>(g0, g1);
                     pk[2 * v + 1] = pack2<kBf16>(g2, g3);
                 }
@@ -348,18 +357,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->ds_full));
         }
-        // epilogue: dV and scale * dK rows of the keys that exist
+        // epilogue: this half's columns of dV and scale * dK for the keys that exist
         const bool live = kc < p.g.N;
         const size_t row = (size_t)row_index(p.layout, b, hk, live ? kc : 0, p.Hkv, p.g.N);
         if (n_items == 0) {
             if (live) {
-                zero_row<D>(p.dv, row);
-                zero_row<D>(p.dk, row);
+                zero_row<D>(p.dv, row, hf);
+                zero_row<D>(p.dk, row, hf);
             }
         } else if (ok && W.wait_warp(smem_u32(&sh->acc_done), 0)) {
             tc_fence_after();
-            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dv, row, 1.f, live);
-            store_row<D, kBf16>(tmem + lane_base + C::kColB, p.dk, row, p.scale, live);
+            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dv, row, hf, 1.f, live);
+            store_row<D, kBf16>(tmem + lane_base + C::kColB, p.dk, row, hf, p.scale, live);
         }
     }
 
@@ -462,12 +471,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         W.drain(smem_u32(&sh->drain), 0);
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------------- dS, epilogue
-        const int wq = warp - kWarpEw0;
+        const int wq = (warp - kWarpEw0) & 3;   // TMEM lane quarter
+        const int hf = (warp - kWarpEw0) >> 2;  // key-column half of the tile
         const int row = wq * 32 + lane;
         const int qi = r0 + row;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS;
-        const uint32_t tDP = tmem + lane_base + C::kColDP;
+        const uint32_t tS = tmem + lane_base + C::kColS + hf * 64;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * 64;
         const size_t vrow = (size_t)bh * p.Npad + qi;
         const float lse2 = p.lse2[vrow];
         const float dsum = p.dsum[vrow];
@@ -477,32 +487,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             const int j = jlo + n;
             if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
             tc_fence_after();
-            uint32_t s[4][32];
-            ld_row128(tS, s);
+            uint32_t s[2][32];
+            ld_half(tS, s);
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->s_free));
             int c_lo = 0, c_hi = kTileN - 1;
             if (tile_needs_mask(p.g, r0, j)) row_visible_cols(p.g, qi, j, c_lo, c_hi);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
+            for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                 for (int v = 0; v < 32; ++v) {
-                    const int col = cc * 32 + v;
+                    const int col = hf * 64 + cc * 32 + v;
                     const float e = ex2(fmaf(u2f(s[cc][v]), c2, -lse2));
                     s[cc][v] = f2u(col < c_lo || col > c_hi ? 0.f : e);
                 }
             if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
             tc_fence_after();
+            uint32_t d[2][32];
+            ld_half(tDP, d);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t d[32];
-                tmem_ld32(tDP + 32 * cc, d);
-                tmem_wait_ld();
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 16; ++v)
-                    pk[v] = pack2<kBf16>(u2f(s[cc][2 * v]) * (u2f(d[2 * v]) - dsum),
-                                         u2f(s[cc][2 * v + 1]) * (u2f(d[2 * v + 1]) - dsum));
+                    pk[v] = pack2<kBf16>(u2f(s[cc][2 * v]) * (u2f(d[cc][2 * v]) - dsum),
+                                         u2f(s[cc][2 * v + 1]) * (u2f(d[cc][2 * v + 1]) - dsum));
                 tmem_st16(tDP + 16 * cc, pk);
             }
             tmem_wait_st();
@@ -512,10 +521,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         const bool live = qi < p.g.N;
         const size_t orow = (size_t)row_index(p.layout, b, h, live ? qi : 0, p.H, p.g.N);
         if (n_items == 0) {
-            if (live) zero_row<D>(p.dq, orow);
+            if (live) zero_row<D>(p.dq, orow, hf);
         } else if (ok && W.wait_warp(smem_u32(&sh->acc_done), 0)) {
             tc_fence_after();
-            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dq, orow, p.scale, live);
+            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dq, orow, hf, p.scale, live);
         }
     }
 
@@ -528,38 +537,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
 }
 
 // ===================================================================== pre
-// Dsum = rowsum(dO * O) and LSE * log2(e) per row, one warp per row, rows
-// past N (up to the padded length) filled so they contribute nothing.
-template <bool kBf16>
+// Dsum = rowsum(dO * O) and LSE * log2(e) per row; D/8 lanes take a row,
+// 16 bytes of O and of dO each, so a warp covers 32/(D/8) whole rows per
+// pass.  Rows past N (up to the padded length) are filled so they contribute
+// nothing.
+template <bool kBf16, int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* o, const uint16_t* d_o, const float* lse,
                                                          float* lse2, float* dsum, int B, int H, int N, int Npad,
-                                                         int D, int layout) {
+                                                         int layout) {
+    constexpr int kLanes = D / 8;
+    constexpr int kRowsPerWarp = 32 / kLanes;
     const long long rows = (long long)B * H * Npad;
     const int lane = threadIdx.x & 31;
-    for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
-         r += ((long long)gridDim.x * blockDim.x) >> 5) {
-        const int i = (int)(r % Npad);
-        const long long bh = r / Npad;
+    const int sub = lane / kLanes;
+    const int l = lane % kLanes;
+    const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kRowsPerWarp; r0 < rows;
+         r0 += warps * kRowsPerWarp) {
+        const long long r = r0 + sub;
         float acc = 0.f;
         float l2 = INFINITY;
-        if (i < N) {
-            const size_t base = (size_t)row_index(layout, (int)(bh / H), (int)(bh % H), i, H, N) * D;
-            for (int e = 2 * lane; e < D; e += 64) {
-                const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base + e);
-                const uint32_t g = *reinterpret_cast<const uint32_t*>(d_o + base + e);
-                acc = fmaf(lo_half<kBf16>(a), lo_half<kBf16>(g), acc);
-                acc = fmaf(hi_half<kBf16>(a), hi_half<kBf16>(g), acc);
+        int i = 0;
+        long long bh = 0;
+        if (r < rows) {
+            i = (int)(r % Npad);
+            bh = r / Npad;
+            if (i < N) {
+                const size_t base = (size_t)row_index(layout, (int)(bh / H), (int)(bh % H), i, H, N) * D + 8 * l;
+                const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+                const uint4 g = *reinterpret_cast<const uint4*>(d_o + base);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+                const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    acc = fmaf(lo_half<kBf16>(aw[m]), lo_half<kBf16>(gw[m]), acc);
+                    acc = fmaf(hi_half<kBf16>(aw[m]), hi_half<kBf16>(gw[m]), acc);
+                }
+                const float lv = lse[bh * N + i];
+                l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
             }
-            const float l = lse[bh * N + i];
-            l2 = l == -INFINITY ? INFINITY : l * kLog2e;
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
+        for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (l == 0 && r < rows) {
             lse2[bh * Npad + i] = l2;
             dsum[bh * Npad + i] = acc;
         }
     }
+}
+
+template <bool kBf16, int D>
+void launch_pre_typed(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B, int H, int N,
+                      int Npad, int layout, int sms, cudaStream_t s) {
+    constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+    const long long rows = (long long)B * H * Npad;
+    long long grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    if (grid > 32LL * sms) grid = 32LL * sms;
+    fa_bwd_pre_kernel<kBf16, D><<<(int)grid, 256, 0, s>>>(static_cast<const uint16_t*>(o),
+                                                          static_cast<const uint16_t*>(d_o), lse, lse2, dsum, B, H,
+                                                          N, Npad, layout);
 }
 
 template <int D, bool kBf16>
@@ -582,17 +618,18 @@ cudaError_t launch_bwd_typed(const BwdParams& p, int B, cudaStream_t s) {
 
 cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B, int H,
                            int N, int Npad, int D, int layout, int dtype_code, int sms, cudaStream_t s) {
-    const long long rows = (long long)B * H * Npad;
-    long long grid = (rows * 32 + 255) / 256;
-    if (grid > 16LL * sms) grid = 16LL * sms;
-    if (dtype_code == 1)
-        fa_bwd_pre_kernel<true><<<(int)grid, 256, 0, s>>>(static_cast<const uint16_t*>(o),
-                                                            static_cast<const uint16_t*>(d_o), lse, lse2, dsum, B, H,
-                                                            N, Npad, D, layout);
-    else
-        fa_bwd_pre_kernel<false><<<(int)grid, 256, 0, s>>>(static_cast<const uint16_t*>(o),
-                                                             static_cast<const uint16_t*>(d_o), lse, lse2, dsum, B, H,
-                                                             N, Npad, D, layout);
+    const bool bf16 = dtype_code == 1;
+    if (D == 64) {
+        if (bf16)
+            launch_pre_typed<true, 64>(o, d_o, lse, lse2, dsum, B, H, N, Npad, layout, sms, s);
+        else
+            launch_pre_typed<false, 64>(o, d_o, lse, lse2, dsum, B, H, N, Npad, layout, sms, s);
+    } else {
+        if (bf16)
+            launch_pre_typed<true, 128>(o, d_o, lse, lse2, dsum, B, H, N, Npad, layout, sms, s);
+        else
+            launch_pre_typed<false, 128>(o, d_o, lse, lse2, dsum, B, H, N, Npad, layout, sms, s);
+    }
     return cudaGetLastError();
 }
 

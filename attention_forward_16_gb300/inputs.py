@@ -45,6 +45,7 @@ class Workload:
     seed: int = 0
     rope: str = ""            # "" (none), "half" or "interleaved": rotary embedding of Q and K first
     rope_base: float = 10000.0
+    backward: bool = False    # the step is the backward pass (dQ, dK, dV) for a random upstream dO
     notes: str = field(default="", compare=False)
 
 
@@ -61,6 +62,13 @@ WORKLOADS = {
     # the benchmark shape with the rotary embedding of Q and K in the step
     "f16_rope_full_4k": Workload("f16_rope_full_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128), MASK_NONE,
                                  seed=1003, rope="half", rope_base=10000.0),
+    # backward pass at the benchmark shape (dO drawn like Q)
+    "f16_bwd_full_4k": Workload("f16_bwd_full_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128), MASK_NONE,
+                                seed=1003, backward=True),
+    "f16_bwd_causal_4k": Workload("f16_bwd_causal_4k", 4, 32, 4096, 128, "f16", 1.0 / math.sqrt(128),
+                                  MASK_CAUSAL, seed=1004, backward=True),
+    "bf16_bwd_causal_4k": Workload("bf16_bwd_causal_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128),
+                                   MASK_CAUSAL, seed=1004, backward=True),
     # causal with the 500000 rotary base of the Llama-3 models the pages run
     "bf16_rope_causal_4k": Workload("bf16_rope_causal_4k", 4, 32, 4096, 128, "bf16", 1.0 / math.sqrt(128),
                                     MASK_CAUSAL, seed=1004, rope="half", rope_base=500000.0),

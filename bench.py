@@ -518,6 +518,188 @@ def run_decode(args, w, world, rank, local, pg):
     return 0
 
 
+# ---------------------------------------------------------------- backward
+
+METRIC_BWD = "fused attention bwd TFLOP/s (5-product count) and % of GB300 dense FP16 tensor peak"
+
+
+def make_upstream(w):
+    """The upstream gradient dO of a backward workload: drawn like Q, seed + 1."""
+    from attention_forward_16_gb300.inputs import make_qkv
+    return make_qkv(w.B, w.H, w.N, w.D, w.dtype, seed=w.seed + 1, input_scale=w.input_scale, n_k=1)[0]
+
+
+def oracle_bwd_sample(w, q, k, v, do, r0, rows):
+    """The oracle's backward for `rows` query rows of one head (their dQ and
+    their contributions to dK, dV); returns the 5-product flops it covers."""
+    from oracle import attention_backward
+    from attention_forward_16_gb300.flops import visible_keys_per_row
+    attention_backward(q[:, :, r0:r0 + rows], k, v, do[:, :, r0:r0 + rows], w.scale, w.mask, w.win_l, w.win_r,
+                       q_offset=r0)
+    per_row = visible_keys_per_row(w.N, w.mask, w.win_l, w.win_r)
+    return 10 * w.D * int(per_row[r0:r0 + rows].sum())
+
+
+def run_backward(args, w, world, rank, local, pg):
+    """Backward pass: one fa_bwd call (pre-pass, dK/dV kernel, dQ kernel) per
+    step for fixed Q, K, V, O, LSE and dO resident in HBM."""
+    import torch
+    import attention_forward_16_gb300 as fa
+    from attention_forward_16_gb300.build import build
+    from attention_forward_16_gb300.flops import attention_flops
+    from attention_forward_16_gb300.inputs import make_workload
+
+    build()
+    fa.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    q, k, v = make_workload(w)
+    do_h = make_upstream(w)
+    dq_, dk_, dv_, ddo = (t.to(device) for t in (q, k, v, do_h))
+    window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
+    causal = w.mask == fa.FA_MASK_CAUSAL
+    stream = torch.cuda.current_stream(device)
+    o, lse = fa.attention_fwd(dq_, dk_, dv_, scale=w.scale, causal=causal, window=window)
+    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=device)
+
+    def step(aq=dq_, ak=dk_, av=dv_, ao=o, al=lse, ado=ddo, s_=None):
+        fa.attention_bwd(aq, ak, av, ao, al, ado, scale=w.scale, causal=causal, window=window, dq=gq, dk=gk,
+                         dv=gv, workspace=ws, stream=s_)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+    clocks = ClockSampler(local).start() if rank == 0 else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(pg, device)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    clk = clocks.stop() if clocks else None
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("kernel reported a timeout during the timed steps")
+    total_ms = reduce_max(pg, t0.elapsed_time(t1), device)
+    call_ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in ev) / args.steps, device)
+    flops_step = 2.5 * attention_flops(w.B, w.H, w.N, w.D, w.mask, w.win_l, w.win_r)
+    value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+
+    # end to end: inputs from pinned host memory, gradients back, every step
+    hin = [t.pin_memory() for t in (q, k, v, o.cpu(), lse.cpu(), do_h)]
+    bins = [torch.empty_like(t, device=device) for t in hin]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (gq, gk, gv)]
+
+    def e2e_step():
+        for dst, src in zip(bins, hin):
+            dst.copy_(src, non_blocking=True)
+        step(*bins[:3], bins[3], bins[4], bins[5])
+        for dst, src in zip(hout, (gq, gk, gv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(pg, e0.elapsed_time(e1), device)
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError("kernel reported a timeout during the end-to-end steps")
+    if rank != 0:
+        return 0
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    achieved = flops_step / (call_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "mask": w.mask,
+                   "window": [w.win_l, w.win_r], "scale": w.scale, "pass": "backward",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "working set (Q, K, V, O, dO and the three gradients) exceeds L2; no flush",
+                   "flops": "5 products (S, dP, dV, dK, dQ) of 2 N_visible D each; the kernels execute 7 "
+                            "(the dQ kernel recomputes S and dP)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "fa_bwd call: fa_bwd_pre_kernel + fa_bwd_dkdv_kernel + fa_bwd_dq_kernel",
+                     "algorithmic_flops_per_launch": flops_step, "avg_launch_ms": call_ms,
+                     "peak_source": peak_src},
+        "clocks": clk,
+        "e2e": {"value": flops_step * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
+                "how": "attention_bwd on host Q, K, V, O, LSE, dO: pinned H2D, backward, D2H of dQ, dK, dV"},
+        "gpu_launches": 3 * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        qd, kd, vd, dd = (t.float().numpy() for t in (q, k, v, do_h))
+        done, t_total, n = 0, 0.0, 0
+        while t_total < args.cpu_seconds and n < w.B * w.H:
+            b, h = divmod(n, w.H)
+            r0 = (n * 977) % (w.N - 64 + 1)
+            t_s = time.perf_counter()
+            done += oracle_bwd_sample(w, qd[b:b + 1, h:h + 1], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                                      dd[b:b + 1, h:h + 1], r0, 64)
+            t_total += time.perf_counter() - t_s
+            n += 1
+        line["cpu_baseline"] = {"value": done / t_total / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n} heads x 64 query rows (their dQ and dK, dV contributions) of "
+                                          f"{w.name}, float64 numpy, {t_total:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_bwd(args, w, world, rank):
+    if rank != 0:
+        return 0
+    from attention_forward_16_gb300.inputs import make_workload
+    q, k, v = make_workload(w)
+    qd, kd, vd, dd = (t.float().numpy() for t in (q, k, v, make_upstream(w)))
+    rows = 64
+
+    def step(i):
+        b, h = divmod(i % (w.B * w.H), w.H)
+        r0 = (i * 977) % (w.N - rows + 1)
+        return oracle_bwd_sample(w, qd[b:b + 1, h:h + 1], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                                 dd[b:b + 1, h:h + 1], r0, rows)
+
+    for i in range(args.warmup):
+        step(i)
+    flops_total = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops_total += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops_total / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype_in": w.dtype,
+                   "mask": w.mask, "window": [w.win_l, w.win_r], "pass": "backward",
+                   "step": f"{rows} query rows of one head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"{rows} query rows x full keys of one (b, h) per step, float64 numpy"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from attention_forward_16_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
@@ -535,8 +717,8 @@ def main(argv=None):
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":
-            return run_reference(args, w, world, rank)
-        return run_native(args, w, world, rank, local, pg)
+            return (run_reference_bwd if w.backward else run_reference)(args, w, world, rank)
+        return (run_backward if w.backward else run_native)(args, w, world, rank, local, pg)
     finally:
         if pg is not None:
             pg.destroy_process_group()
