@@ -25,6 +25,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -259,6 +260,230 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
     }
 }
 
+// Eight consecutive elements of a row as fp32.
+template <typename T>
+struct Row8 {
+    using raw = uint4;  // 8 x 16-bit
+    static __device__ __forceinline__ raw load(const T* p) { return *reinterpret_cast<const uint4*>(p); }
+    static __device__ __forceinline__ void cvt(const raw& r, float* f) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                f[2 * i] = __uint_as_float(w[i] << 16);
+                f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            } else {
+                f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFFu)));
+                f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+            }
+        }
+    }
+};
+template <>
+struct Row8<float> {
+    struct raw {
+        float4 a, b;
+    };
+    static __device__ __forceinline__ raw load(const float* p) {
+        return raw{reinterpret_cast<const float4*>(p)[0], reinterpret_cast<const float4*>(p)[1]};
+    }
+    static __device__ __forceinline__ void cvt(const raw& r, float* f) {
+        f[0] = r.a.x, f[1] = r.a.y, f[2] = r.a.z, f[3] = r.a.w, f[4] = r.b.x, f[5] = r.b.y, f[6] = r.b.z, f[7] = r.b.w;
+    }
+};
+
+// Sum of four rows' partial dot products over the L lanes of a lane group,
+// transposed: the first two steps exchange half of the remaining rows
+// instead of all of them, so 4 rows cost L/8 + 4 shuffles rather than
+// 4 log2(L).  Afterwards lane t holds the full sum of row
+// 2 * ((t / (L/2)) & 1) + ((t / (L/4)) & 1); lane r * (L/4) holds row r.
+template <int L>
+__device__ __forceinline__ float reduce_rows4(const float (&d)[4], int t) {
+    constexpr int B1 = L / 2, B2 = L / 4;
+    const bool h1 = t & B1;
+    float k0 = h1 ? d[2] : d[0], k1 = h1 ? d[3] : d[1];
+    k0 += __shfl_xor_sync(0xffffffffu, h1 ? d[0] : d[2], B1);
+    k1 += __shfl_xor_sync(0xffffffffu, h1 ? d[1] : d[3], B1);
+    const bool h2 = t & B2;
+    float v = h2 ? k1 : k0;
+    v += __shfl_xor_sync(0xffffffffu, h2 ? k0 : k1, B2);
+#pragma unroll
+    for (int off = B2 / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Two to four query rows per (batch, K/V head) -- grouped heads, or a few
+// new tokens.  A key row is split over L = D/8 lanes (16 bytes each for
+// 16-bit types), so a warp takes 32/L keys side by side; each lane group
+// keeps its own online-softmax state for the keys it sees, and all groups of
+// the CTA merge at the end.  Against one key per warp with a five-step
+// butterfly per row, this cuts the shuffles per key and row from 5 to about 1.
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const DecodeParams p) {
+    using R8 = Row8<T>;
+    constexpr int L = D / 8;                        // lanes per key
+    constexpr int KPW = 32 / L;                     // keys side by side in a warp
+    constexpr int U = sizeof(T) == 4 ? 2 : 4;       // keys per lane group per iteration
+    constexpr int kBlock = KPW * U;                 // keys per warp per iteration
+    constexpr int kStates = kDecWarps * KPW;
+    constexpr int DV = D / 32;
+    extern __shared__ float dsm[];                  // [kStates][4][D + 2]: m, l, acc
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / L;
+    const int t = lane % L;
+    const int split = blockIdx.x % p.n_splits;
+    const long long bh = blockIdx.x / p.n_splits;
+    const int k0 = split * p.chunk;
+    const int k1 = min(p.Nk, k0 + p.chunk);
+    const int rows = p.G * p.Nq;
+    const T* qg = static_cast<const T*>(p.q);
+    const T* kg = static_cast<const T*>(p.k);
+    const T* vg = static_cast<const T*>(p.v);
+
+    float q[4][8], acc[4][8], m[4], l[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
+        if (r < rows) {
+            R8::cvt(R8::load(qg + dec_qrow(p, bh, r, D) + t * 8), q[r]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[r][e] *= p.scale_log2;  // scores in log2 units
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q[r][e] = 0.f;
+        }
+    }
+
+    // Masks only matter if some query does not see the whole key chunk
+    // (decode's usual case, every cached key visible, skips the per-key test).
+    bool all_vis = true;
+    for (int i = 0; i < p.Nq; ++i) all_vis = all_vis && dec_visible(p, i, k0) && dec_visible(p, i, k1 - 1);
+
+    // key u of a block for this lane group: base + u * KPW + grp, so one load
+    // instruction of the warp reads KPW consecutive rows
+    typename R8::raw kn[U], vn[U];
+    auto load_block = [&](int base) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            int j = base + u * KPW + grp;
+            if (j >= k1) j = k1 - 1;  // clamp: tail keys are masked below
+            const size_t off = dec_krow(p, bh, j, D) + t * 8;
+            kn[u] = R8::load(kg + off);
+            vn[u] = R8::load(vg + off);
+        }
+    };
+    constexpr int kStride = kDecWarps * kBlock;
+    if (k0 + warp * kBlock < k1) load_block(k0 + warp * kBlock);
+    for (int base = k0 + warp * kBlock; base < k1; base += kStride) {
+        typename R8::raw vr[U];
+        float sc[U][4];
+        // scores of the group's U keys for all four rows: U independent dot
+        // products and shuffle chains
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float kf[8];
+            R8::cvt(kn[u], kf);
+            vr[u] = vn[u];
+            float d[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float a = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a = fmaf(q[r][e], kf[e], a);
+                d[r] = a;
+            }
+            const float own = reduce_rows4<L>(d, t);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[u][r] = __shfl_sync(0xffffffffu, own, grp * L + r * (L / 4));
+        }
+        if (base + kStride < k1) load_block(base + kStride);
+        const bool full_block = all_vis && base + kBlock <= k1;
+        if (!full_block) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = base + u * KPW + grp;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    if (j >= k1 || !dec_visible(p, r % p.Nq, j)) sc[u][r] = -INFINITY;
+            }
+        }
+        float vf[U][8];
+#pragma unroll
+        for (int u = 0; u < U; ++u) R8::cvt(vr[u], vf[u]);
+        // online softmax, one max and one rescale check per row per U keys
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if (r >= rows) break;
+            float mx = sc[0][r];
+#pragma unroll
+            for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][r]);
+            if (mx == -INFINITY) continue;
+            if (mx > m[r]) {
+                const float a = m[r] == -INFINITY ? 0.f : ptx::ex2(m[r] - mx);
+                l[r] *= a;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r][e] *= a;
+                m[r] = mx;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float pr = ptx::ex2(sc[u][r] - m[r]);
+                l[r] += pr;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r][e] = fmaf(pr, vf[u][e], acc[r][e]);
+            }
+        }
+    }
+
+    // Merge the kStates lane-group states through shared memory.
+    float* mine = dsm + (size_t)(warp * KPW + grp) * 4 * (D + 2);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (r >= rows) break;
+        if (t == 0) {
+            mine[r * (D + 2) + D] = m[r];
+            mine[r * (D + 2) + D + 1] = l[r];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mine[r * (D + 2) + t * 8 + e] = acc[r][e];
+    }
+    __syncthreads();
+    for (int i = warp; i < rows; i += kDecWarps) {
+        float M = -INFINITY;
+        for (int w = 0; w < kStates; ++w) M = fmaxf(M, dsm[((size_t)w * 4 + i) * (D + 2) + D]);
+        float Lsum = 0.f, o[DV];
+#pragma unroll
+        for (int e = 0; e < DV; ++e) o[e] = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kStates; ++w) {
+                const float* st = dsm + ((size_t)w * 4 + i) * (D + 2);
+                const float a = st[D] == -INFINITY ? 0.f : ptx::ex2(st[D] - M);
+                Lsum += a * st[D + 1];
+#pragma unroll
+                for (int e = 0; e < DV; ++e) o[e] = fmaf(a, st[lane * DV + e], o[e]);
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kDecLn2 : -INFINITY;
+        if (p.n_splits == 1) {
+            T* ob = static_cast<T*>(p.o) + dec_qrow(p, bh, i, D) + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(o[e] * inv);
+            if (p.lse && lane == 0) p.lse[(size_t)bh * rows + i] = lse;
+        } else {
+            const size_t prow = ((size_t)bh * p.n_splits + split) * rows + i;
+            float* po = p.part_o + prow * D + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) po[e] = o[e] * inv;
+            if (lane == 0) p.part_lse[prow] = lse;
+        }
+    }
+}
+
 // One warp per output row: O = sum_s e^{LSE_s - LSE} O_s.
 template <typename T, int DV>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
@@ -309,12 +534,25 @@ cudaError_t launch_split(const DecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Query count buckets keep the per-row register arrays no larger than needed.
+template <typename T, int D>
+cudaError_t launch_rows(const DecodeParams& p, cudaStream_t s) {
+    const long long blocks = (long long)p.BH * p.n_splits;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(float) * kDecWarps * (32 / (D / 8)) * 4 * (D + 2);
+    auto kern = fa_decode_rows_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)blocks, kDecThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Query count buckets keep the per-row register arrays no larger than needed;
+// two to four rows take the lane-group kernel.
 template <typename T, int DV>
 cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
     const int rows = p.G * p.Nq;
     cudaError_t e = rows == 1   ? launch_split<T, DV, 1>(p, s)
-                    : rows <= 4 ? launch_split<T, DV, 4>(p, s)
+                    : rows <= 4 ? launch_rows<T, 32 * DV>(p, s)
                                 : launch_split<T, DV, kDecodeMaxQ>(p, s);
     if (e != cudaSuccess || p.n_splits == 1) return e;
     const long long all_rows = (long long)p.BH * rows;
