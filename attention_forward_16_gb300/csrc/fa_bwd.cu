@@ -303,8 +303,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             tc_fence_after();
             uint32_t s[2][32];
             ld_half(tS, s);
+            const bool masked = tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
             int r_lo = 0, r_hi = kTileM - 1;
-            if (tile_needs_mask(p.g, i * kTileM, j)) key_visible_rows(p.g, kc, i, r_lo, r_hi);
+            if (masked) key_visible_rows(p.g, kc, i, r_lo, r_hi);
             // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -312,15 +313,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const float4 l4 = lse2[cc * 8 + v];
-                    const int q = hf * 64 + cc * 32 + 4 * v;
-                    float e0 = ex2(fmaf(u2f(s[cc][4 * v]), c2, -l4.x));
-                    float e1 = ex2(fmaf(u2f(s[cc][4 * v + 1]), c2, -l4.y));
-                    float e2 = ex2(fmaf(u2f(s[cc][4 * v + 2]), c2, -l4.z));
-                    float e3 = ex2(fmaf(u2f(s[cc][4 * v + 3]), c2, -l4.w));
-                    if (q < r_lo || q > r_hi) e0 = 0.f;
-                    if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
-                    if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
-                    if (q + 3 < r_lo || q + 3 > r_hi) e3 = 0.f;
+                    float e0, e1, e2, e3;
+                    ffma2(e0, e1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]), c2, c2, -l4.x, -l4.y);
+                    ffma2(e2, e3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]), c2, c2, -l4.z, -l4.w);
+                    e0 = ex2(e0);
+                    e1 = ex2(e1);
+                    e2 = ex2(e2);
+                    e3 = ex2(e3);
+                    if (masked) {
+                        const int q = hf * 64 + cc * 32 + 4 * v;
+                        if (q < r_lo || q > r_hi) e0 = 0.f;
+                        if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
+                        if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
+                        if (q + 3 < r_lo || q + 3 > r_hi) e3 = 0.f;
+                    }
                     s[cc][4 * v] = f2u(e0);
                     s[cc][4 * v + 1] = f2u(e1);
                     s[cc][4 * v + 2] = f2u(e2);
@@ -344,10 +350,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
                     const float4 d4 = dsum[cc * 8 + v];
-                    const float g0 = u2f(s[cc][4 * v]) * (u2f(d[cc][4 * v]) - d4.x);
-                    const float g1 = u2f(s[cc][4 * v + 1]) * (u2f(d[cc][4 * v + 1]) - d4.y);
-                    const float g2 = u2f(s[cc][4 * v + 2]) * (u2f(d[cc][4 * v + 2]) - d4.z);
-                    const float g3 = u2f(s[cc][4 * v + 3]) * (u2f(d[cc][4 * v + 3]) - d4.w);
+                    float g0, g1, g2, g3;
+                    fadd2(g0, g1, u2f(d[cc][4 * v]), u2f(d[cc][4 * v + 1]), -d4.x, -d4.y);
+                    fadd2(g2, g3, u2f(d[cc][4 * v + 2]), u2f(d[cc][4 * v + 3]), -d4.z, -d4.w);
+                    fmul2(g0, g1, g0, g1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]));
+                    fmul2(g2, g3, g2, g3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]));
                     pk[2 * v] = pack2<kBf16>(g0, g1);
                     pk[2 * v + 1] = pack2<kBf16>(g2, g3);
                 }
@@ -491,15 +498,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             ld_half(tS, s);
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->s_free));
+            const bool masked = tile_needs_mask(p.g, r0, j);  // uniform over the CTA
             int c_lo = 0, c_hi = kTileN - 1;
-            if (tile_needs_mask(p.g, r0, j)) row_visible_cols(p.g, qi, j, c_lo, c_hi);
+            if (masked) row_visible_cols(p.g, qi, j, c_lo, c_hi);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                for (int v = 0; v < 32; ++v) {
-                    const int col = hf * 64 + cc * 32 + v;
-                    const float e = ex2(fmaf(u2f(s[cc][v]), c2, -lse2));
-                    s[cc][v] = f2u(col < c_lo || col > c_hi ? 0.f : e);
+                for (int v = 0; v < 32; v += 2) {
+                    float e0, e1;
+                    ffma2(e0, e1, u2f(s[cc][v]), u2f(s[cc][v + 1]), c2, c2, -lse2, -lse2);
+                    e0 = ex2(e0);
+                    e1 = ex2(e1);
+                    if (masked) {
+                        const int col = hf * 64 + cc * 32 + v;
+                        if (col < c_lo || col > c_hi) e0 = 0.f;
+                        if (col + 1 < c_lo || col + 1 > c_hi) e1 = 0.f;
+                    }
+                    s[cc][v] = f2u(e0);
+                    s[cc][v + 1] = f2u(e1);
                 }
             if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
             tc_fence_after();
@@ -509,9 +525,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int v = 0; v < 16; ++v)
-                    pk[v] = pack2<kBf16>(u2f(s[cc][2 * v]) * (u2f(d[cc][2 * v]) - dsum),
-                                         u2f(s[cc][2 * v + 1]) * (u2f(d[cc][2 * v + 1]) - dsum));
+                for (int v = 0; v < 16; ++v) {
+                    float g0, g1;
+                    fadd2(g0, g1, u2f(d[cc][2 * v]), u2f(d[cc][2 * v + 1]), -dsum, -dsum);
+                    fmul2(g0, g1, g0, g1, u2f(s[cc][2 * v]), u2f(s[cc][2 * v + 1]));
+                    pk[v] = pack2<kBf16>(g0, g1);
+                }
                 tmem_st16(tDP + 16 * cc, pk);
             }
             tmem_wait_st();
