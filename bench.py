@@ -350,6 +350,9 @@ def run_native(args, w, world, rank, local, pg):
         raise RuntimeError("kernel reported a timeout during the timed steps")
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    launch_sorted = sorted(launch_ms)
+    launch_stats = {"median_ms": launch_sorted[len(launch_sorted) // 2], "min_ms": launch_sorted[0],
+                    "max_ms": launch_sorted[-1]}
     total_ms = reduce_max(pg, total_ms, device)
     avg_launch_ms = reduce_max(pg, sum(launch_ms) / len(launch_ms), device)
     rope_ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in rev) / len(rev), device) if rope else None
@@ -428,7 +431,7 @@ def run_native(args, w, world, rank, local, pg):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "fa_fwd_tc_kernel<%d,%s>" % (w.D, w.dtype),
                      "algorithmic_flops_per_launch": flops_step,
-                     "avg_launch_ms": avg_launch_ms, "peak_source": peak_src},
+                     "avg_launch_ms": avg_launch_ms, "launch_ms": launch_stats, "peak_source": peak_src},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
