@@ -19,6 +19,8 @@ FlashAttention reproduces exactly:
   practice", section "The core idea of FlashAttention: IO-aware"
   (``standard_attention``: matmul, softmax over the last axis, matmul).
 
+``paged.py`` gathers a sequence's keys and values from a paged cache (the
+first page's section 9) and applies the same definition to them.
 ``backward.py`` gives the gradients of that definition with respect to Q, K
 and V (the chain rule through it), for the backward pass the second page
 says the operator also has.  ``rope.py`` adds the rotary position embedding that the first page's
@@ -43,6 +45,7 @@ from .attention import (  # noqa: F401
     unmasked_pairs,
 )
 from .backward import attention_backward, attention_backward_grouped  # noqa: F401
+from .paged import attention_paged, gather_pages  # noqa: F401
 from .rope import (  # noqa: F401
     STYLE_HALF,
     STYLE_INTERLEAVED,
