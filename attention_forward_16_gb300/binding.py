@@ -46,6 +46,8 @@ SIGNATURES = {
     "fa_decode_plan_gqa": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_decode_gqa": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _I, _P,
                            ctypes.c_ulonglong, _P]),
+    "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I,
+                             _I, _I, _P, ctypes.c_ulonglong, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P]),
     "fa_decode_noalloc_scratch_bytes": (ctypes.c_ulonglong, []),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _P,
@@ -148,6 +150,14 @@ def fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, 
               workspace_bytes, stream):
     return load().fa_decode(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits,
                             workspace, workspace_bytes, stream)
+
+
+def fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, H_kv, Nq, max_seq_len, page_size,
+                    max_pages, num_pages, D, scale, mask_kind, win_l, win_r, dtype, layout, n_splits, workspace,
+                    workspace_bytes, stream):
+    return load().fa_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H, H_kv, Nq, max_seq_len,
+                                  page_size, max_pages, num_pages, D, scale, mask_kind, win_l, win_r, dtype, layout,
+                                  n_splits, workspace, workspace_bytes, stream)
 
 
 def fa_decode_noalloc(q, k, v, o, lse, B, H, Nq, Nk, D, scale, mask_kind, win_l, win_r, dtype, n_splits, stream):
@@ -435,6 +445,58 @@ def attention_fwd_rope(q, k, v, cos, sin, style="half", pos0=0, layout="bhnd", *
     qr, kr = apply_rope(q, k, cos, sin, style=style, q_pos0=pos0, k_pos0=pos0, layout=layout,
                         stream=kw.get("stream"))
     return attention_fwd(qr, kr, v, layout=layout, **kw)
+
+
+def attention_decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len=None, scale=None, causal=False,
+                           window=None, n_splits=0, out=None, lse=None, workspace=None, stream=None, layout="bhnd"):
+    """Decode against a paged cache: k_cache, v_cache [num_pages, page_size,
+    H_kv, D]; block_table int32 [B, max_pages]; seq_lens int32 [B] (all CUDA).
+    Query i of sequence b sits at position seq_lens[b] - Nq + i.  q is
+    [B, H, Nq, D] (``layout="bhnd"``) or [B, Nq, H, D].  ``max_seq_len`` (the
+    split plan's length, at least every seq_lens[b]) defaults to
+    max_pages * page_size.  Returns (O, LSE), LSE [B, H, Nq]."""
+    if layout not in _LAYOUT_CODE:
+        raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must be [num_pages, page_size, H_kv, D] alike")
+    num_pages, page_size, Hkv, D = k_cache.shape
+    if layout == "bhnd":
+        B, H, Nq, Dq = q.shape
+    else:
+        B, Nq, H, Dq = q.shape
+    if Dq != D or H % Hkv:
+        raise ValueError("q does not match the cache's head size or K/V head count")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise ValueError("seq_lens must be int32 [B]")
+    for t in (q, k_cache, v_cache, block_table, seq_lens):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("all inputs must be contiguous CUDA tensors")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype) or q.dtype not in _DTYPE_CODE:
+        raise ValueError("q and the caches must share one dtype among float16, bfloat16, float32")
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * page_size
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mk, wl, wr = mask_args(causal, window)
+    with torch.cuda.device(q.device):
+        ns, wb = fa_decode_plan_gqa(B, H, Hkv, Nq, max_seq_len, D, n_splits)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        if workspace is None and wb > 0:
+            workspace = torch.empty(wb, dtype=torch.uint8, device=q.device)
+        s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+        rc = fa_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                             seq_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, Nq, max_seq_len,
+                             page_size, max_pages, num_pages, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype],
+                             _LAYOUT_CODE[layout], ns, workspace.data_ptr() if workspace is not None else None,
+                             workspace.numel() if workspace is not None else 0, s)
+    _check(rc, "fa_decode_paged")
+    return out, lse
 
 
 def attention_fwd_host(q, k, v, device="cuda", **kw):

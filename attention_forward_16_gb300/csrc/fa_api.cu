@@ -348,6 +348,68 @@ int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* l
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                    const int* seq_lens, void* o, float* lse, int B, int H, int H_kv, int Nq, int max_seq_len,
+                    int page_size, int max_pages, int num_pages, int D, float scale, int mask_kind, int win_l,
+                    int win_r, int dtype, int layout, int n_splits, void* workspace,
+                    unsigned long long workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return FA_ERR_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || D <= 0 || max_seq_len <= 0 || max_pages <= 0 || num_pages <= 0)
+        return FA_ERR_ARG;
+    if (page_size <= 0 || (page_size & (page_size - 1)) != 0) return FA_ERR_ARG;
+    if ((long long)max_pages * page_size < max_seq_len) return FA_ERR_ARG;
+    if ((long long)num_pages * page_size * H_kv * D > (1LL << 46)) return FA_ERR_ARG;
+    if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
+    if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_ARG;
+    fa::Geom g;
+    int rc = normalise_mask(mask_kind, win_l, win_r, max_seq_len, &g);
+    if (rc != FA_OK) return rc;
+    if ((long long)B * H > 0x7fffffffLL) return FA_ERR_ARG;
+    const int G = H / H_kv;
+    if (dtype < FA_F16 || dtype > FA_F32 || (D != 64 && D != 128) || (long long)G * Nq > fa::kDecodeMaxQ)
+        return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16)) return FA_ERR_ALIGN;
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4))) return FA_ERR_ALIGN;
+    DeviceInfo* dev;
+    if ((rc = device_info(&dev)) != FA_OK) return rc;
+    fa::DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.BH = (long long)B * H_kv;
+    p.G = G;
+    p.Hkv = H_kv;
+    p.layout = layout;
+    fa::decode_plan(p.BH, max_seq_len, dev->sms, n_splits, &p.n_splits, &p.chunk);
+    const unsigned long long need = fa::decode_workspace_bytes(p.BH, G * Nq, D, p.n_splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return FA_ERR_ARG;
+        if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+        p.part_o = static_cast<float*>(workspace);
+        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              ((unsigned long long)p.BH * p.n_splits * G * Nq * D * 4 + 255) / 256 * 256);
+    }
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.o = o;
+    p.lse = lse;
+    p.Nq = Nq;
+    p.Nk = max_seq_len;
+    p.D = D;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.win_l = g.win_l;
+    p.win_r = g.win_r;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    int shift = 0;
+    while ((1 << shift) < page_size) ++shift;
+    p.page_shift = shift;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    cudaError_t e = fa::launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
               float scale, int mask_kind, int win_l, int win_r, int dtype, int n_splits, void* workspace,
               unsigned long long workspace_bytes, void* stream) {

@@ -102,13 +102,29 @@ __device__ __forceinline__ size_t dec_qrow(const DecodeParams& p, long long bhk,
     return (((size_t)b * p.Nq + i) * ((size_t)p.Hkv * p.G) + h) * D;
 }
 __device__ __forceinline__ size_t dec_krow(const DecodeParams& p, long long bhk, int j, int D) {
+    if (p.block_table) {
+        // paged: [num_pages, page_size, Hkv, D]; a bad page index is clamped, never followed
+        const long long b = bhk / p.Hkv, hk = bhk % p.Hkv;
+        int page = p.block_table[(size_t)b * p.max_pages + (j >> p.page_shift)];
+        page = page < 0 ? 0 : (page >= p.num_pages ? p.num_pages - 1 : page);
+        const int r = j & ((1 << p.page_shift) - 1);
+        return ((((size_t)page << p.page_shift) + r) * p.Hkv + hk) * D;
+    }
     if (p.layout == LAYOUT_BHND) return ((size_t)bhk * p.Nk + j) * D;
     const long long b = bhk / p.Hkv, hk = bhk % p.Hkv;
     return (((size_t)b * p.Nk + j) * p.Hkv + hk) * D;
 }
 
-__device__ __forceinline__ bool dec_visible(const DecodeParams& p, int i, int j) {
-    const long long pos = (long long)p.Nk - p.Nq + i;
+// Cached positions of the sequence of (batch, K/V head) group bhk.
+__device__ __forceinline__ int dec_len(const DecodeParams& p, long long bhk) {
+    if (!p.seq_lens) return p.Nk;
+    const int n = p.seq_lens[bhk / p.Hkv];
+    return n < 0 ? 0 : (n > p.Nk ? p.Nk : n);
+}
+
+// Query i of a sequence of `len` cached positions sits at len - Nq + i.
+__device__ __forceinline__ bool dec_visible(const DecodeParams& p, int i, int j, int len) {
+    const long long pos = (long long)len - p.Nq + i;
     if (p.win_l >= 0 && j < pos - p.win_l) return false;
     if (p.win_r >= 0 && j > pos + p.win_r) return false;
     return true;
@@ -124,8 +140,9 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.n_splits;
     const long long bh = blockIdx.x / p.n_splits;
+    const int len = dec_len(p, bh);
     const int k0 = split * p.chunk;
-    const int k1 = min(p.Nk, k0 + p.chunk);
+    const int k1 = min(len, k0 + p.chunk);
     const int rows = p.G * p.Nq;
     const T* qg = static_cast<const T*>(p.q);
     const T* kg = static_cast<const T*>(p.k);
@@ -194,7 +211,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
             float mx = -INFINITY;
 #pragma unroll
             for (int u = 0; u < kKeysPerIter; ++u) {
-                if (base + u >= k1 || !dec_visible(p, i % p.Nq, base + u)) s[u] = -INFINITY;
+                if (base + u >= k1 || !dec_visible(p, i % p.Nq, base + u, len)) s[u] = -INFINITY;
                 mx = fmaxf(mx, s[u]);
             }
             if (mx == -INFINITY) continue;  // warp-uniform: no visible key in this group
@@ -334,8 +351,9 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
     const int t = lane % L;
     const int split = blockIdx.x % p.n_splits;
     const long long bh = blockIdx.x / p.n_splits;
+    const int len = dec_len(p, bh);
     const int k0 = split * p.chunk;
-    const int k1 = min(p.Nk, k0 + p.chunk);
+    const int k1 = min(len, k0 + p.chunk);
     const int rows = p.G * p.Nq;
     const T* qg = static_cast<const T*>(p.q);
     const T* kg = static_cast<const T*>(p.k);
@@ -361,7 +379,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
     // Masks only matter if some query does not see the whole key chunk
     // (decode's usual case, every cached key visible, skips the per-key test).
     bool all_vis = true;
-    for (int i = 0; i < p.Nq; ++i) all_vis = all_vis && dec_visible(p, i, k0) && dec_visible(p, i, k1 - 1);
+    for (int i = 0; i < p.Nq; ++i) all_vis = all_vis && dec_visible(p, i, k0, len) && dec_visible(p, i, k1 - 1, len);
 
     // key u of a block for this lane group: base + u * KPW + grp, so one load
     // instruction of the warp reads KPW consecutive rows
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
                 const int j = base + u * KPW + grp;
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    if (j >= k1 || !dec_visible(p, r % p.Nq, j)) sc[u][r] = -INFINITY;
+                    if (j >= k1 || !dec_visible(p, r % p.Nq, j, len)) sc[u][r] = -INFINITY;
             }
         }
         float vf[U][8];

@@ -79,6 +79,14 @@ struct DecodeParams {
     int G = 1;          // query heads per K/V head; a CTA takes all G * Nq query rows of its K/V head
     int Hkv = 1;        // K/V heads (read only for [B, N, H, D])
     int layout = LAYOUT_BHND;
+    // Paged cache (block_table != null): k, v are [num_pages, page_size, Hkv, D];
+    // position j of sequence b is row j % page_size of page block_table[b][j / page_size];
+    // sequence b has seq_lens[b] positions (clamped to [0, Nk]); Nk is the longest.
+    const int* block_table = nullptr;
+    const int* seq_lens = nullptr;
+    int page_shift = 0;  // log2(page_size)
+    int max_pages = 0;   // row stride of block_table
+    int num_pages = 0;   // page indices are clamped to [0, num_pages)
 };
 
 // Split count and key chunk for a decode problem (n_req <= 0: choose).

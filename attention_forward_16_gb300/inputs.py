@@ -91,6 +91,8 @@ class DecodeWorkload:
     win_r: int = -1
     seed: int = 0
     Hkv: int = 0        # K/V heads (0: same as H)
+    page_size: int = 0  # > 0: the cache is paged, its pages shuffled in memory
+
 
 
 DECODE_WORKLOADS = {
@@ -100,7 +102,27 @@ DECODE_WORKLOADS = {
                                           MASK_CAUSAL, seed=1103, Hkv=8),
     "f16_decode_4k_q4": DecodeWorkload("f16_decode_4k_q4", 4, 32, 4, 4096, 128, "f16", 1.0 / math.sqrt(128),
                                        MASK_CAUSAL, seed=1102),
+    # the grouped-head cache above, cut into 256-position pages at shuffled places
+    "bf16_decode_paged_32k": DecodeWorkload("bf16_decode_paged_32k", 8, 32, 1, 32768, 128, "bf16",
+                                            1.0 / math.sqrt(128), MASK_CAUSAL, seed=1103, Hkv=8, page_size=256),
 }
+
+
+def make_paged(w: DecodeWorkload, k, v):
+    """Cut the contiguous cache k, v [B, H_kv, Nk, D] into page_size-position
+    pages [num_pages, page_size, H_kv, D], placed by a seeded permutation;
+    returns (k_cache, v_cache, block_table int32 [B, Nk / page_size])."""
+    B, Hkv, Nk, D = k.shape
+    ps = w.page_size
+    per_seq = Nk // ps
+    perm = torch.from_numpy(np.random.default_rng(w.seed + 7).permutation(B * per_seq).astype(np.int64))
+    def pages(x):
+        x = x.permute(0, 2, 1, 3).reshape(B * per_seq, ps, Hkv, D)   # logical page order
+        out = torch.empty_like(x)
+        out[perm] = x
+        return out.contiguous()
+    table = perm.reshape(B, per_seq).to(torch.int32)
+    return pages(k), pages(v), table
 
 
 def make_decode(w: DecodeWorkload):

@@ -470,6 +470,11 @@ def run_decode(args, w, world, rank, local, pg):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     q, k, v = make_decode(w)
+    if w.page_size:
+        from attention_forward_16_gb300.inputs import make_paged
+        k, v, table = make_paged(w, k, v)
+        dtab = table.to(device)
+        dlens = torch.full((w.B,), w.Nk, dtype=torch.int32, device=device)
     dq, dk, dv = q.to(device), k.to(device), v.to(device)
     do = torch.empty_like(dq)
     dl = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
@@ -480,8 +485,13 @@ def run_decode(args, w, world, rank, local, pg):
     stream = torch.cuda.current_stream(device)
 
     def step():
-        fa.attention_decode(dq, dk, dv, scale=w.scale, causal=w.mask == fa.FA_MASK_CAUSAL, window=window,
-                            out=do, lse=dl, workspace=ws if wb > 0 else None)
+        if w.page_size:
+            fa.attention_decode_paged(dq, dk, dv, dtab, dlens, max_seq_len=w.Nk, scale=w.scale,
+                                      causal=w.mask == fa.FA_MASK_CAUSAL, window=window, out=do, lse=dl,
+                                      workspace=ws if wb > 0 else None)
+        else:
+            fa.attention_decode(dq, dk, dv, scale=w.scale, causal=w.mask == fa.FA_MASK_CAUSAL, window=window,
+                                out=do, lse=dl, workspace=ws if wb > 0 else None)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -509,6 +519,7 @@ def run_decode(args, w, world, rank, local, pg):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": Hkv, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+                   "page_size": w.page_size or None,
                    "mask": w.mask,
                    "n_splits": ns, "workspace_bytes": wb,
                    "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * Hkv * w.Nk * w.D * e >> 20)},

@@ -181,6 +181,35 @@ int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* l
                   void* stream);
 
 /*
+ * fa_decode_paged -- fa_decode_gqa against a paged K/V cache.  "Ascend C
+ * advanced practice: high-performance FlashAttention-2-style tile-level fused
+ * attention", section 9 ("Extensions: integration with RoPE and a paged KV
+ * cache"), replaces the K/V block loads with a gather from a paged cache; the
+ * page gives no format, so this takes the common one:
+ *   k_cache, v_cache: [num_pages, page_size, H_kv, D] (dtype as q);
+ *   block_table: int [B, max_pages]; position j of sequence b is row
+ *     j % page_size of page block_table[b * max_pages + j / page_size];
+ *   seq_lens: int [B]; sequence b has seq_lens[b] cached positions (values
+ *     outside [0, max_seq_len] are clamped), and its Nq new queries sit at
+ *     positions seq_lens[b] - Nq + i, which set the causal and window masks
+ *     (a query whose position is negative sees no key: O = 0, LSE = -inf).
+ * q, o and lse as in fa_decode_gqa (`layout` applies to q and o only).
+ * block_table and seq_lens are device memory the library only reads; a
+ * page index outside [0, num_pages) is clamped, so a bad table gives wrong
+ * values, never an out-of-bounds read.  page_size must be a power of two
+ * with max_pages * page_size >= max_seq_len.  The split plan and workspace are
+ * fa_decode_plan_gqa(B, H, H_kv, Nq, max_seq_len, D, n_splits); splits past a
+ * sequence's length contribute nothing.  Errors as for fa_decode_gqa, plus
+ * FA_ERR_ARG for the page arguments and FA_ERR_ALIGN for a block table or
+ * length array not 4-byte aligned.
+ */
+int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                    const int* seq_lens, void* o, float* lse,
+                    int B, int H, int H_kv, int Nq, int max_seq_len, int page_size, int max_pages, int num_pages,
+                    int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int layout,
+                    int n_splits, void* workspace, unsigned long long workspace_bytes, void* stream);
+
+/*
  * fa_decode_noalloc -- fa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this entry point.  It exists for code that

@@ -161,3 +161,76 @@ def test_decode_grouped_rejects_too_many_rows():
                             None) == fb.FA_ERR_UNSUPPORTED
     assert fb.fa_decode_gqa(p, p, p, p, None, 1, 32, 5, 1, 64, 128, 0.1, 0, -1, -1, fb.FA_F16, 0, 1, None, 0,
                             None) == fb.FA_ERR_ARG
+
+
+# ------------------------------------------------------------- paged cache
+
+def _paged_case(B, H, Hkv, Nq, lens, D, ps, dtype, seed):
+    """Q, a page-shuffled cache holding each sequence's K/V, its table and lengths."""
+    rng = np.random.default_rng(seed)
+    max_pages = -(-max(lens) // ps)
+    num_pages = B * max_pages + 3
+    q, _, _ = make_qkv(B, H, Nq, D, dtype, seed=seed, n_k=1)
+    _, kc, vc = make_qkv(1, num_pages, 1, D * Hkv, dtype, seed=seed + 1, n_k=ps)   # [1, pages, ps, Hkv*D]
+    kc = kc.reshape(num_pages, ps, Hkv, D).contiguous()
+    vc = vc.reshape(num_pages, ps, Hkv, D).contiguous()
+    table = rng.permutation(num_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    return q, kc, vc, table, np.array(lens, dtype=np.int32)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("H,Hkv,Nq", [(4, 4, 1), (8, 2, 1), (8, 2, 3)])
+@pytest.mark.parametrize("ps", [16, 64])
+def test_paged_decode_matches_oracle(dtype, H, Hkv, Nq, ps):
+    from oracle import attention_paged
+    B, D = 3, 128
+    lens = [1000, 37, 2 * ps + 1]
+    q, kc, vc, table, sl = _paged_case(B, H, Hkv, Nq, lens, D, ps, dtype, seed=ps + H + Nq)
+    for mk, wl, wr in MASKS:
+        window = (wl, wr) if mk == MASK_WINDOW else None
+        for ns in (0, 1, 5):
+            o, lse = fa.attention_decode_paged(q.cuda(), kc.cuda(), vc.cuda(), torch.from_numpy(table).cuda(),
+                                               torch.from_numpy(sl).cuda(), scale=0.1, causal=mk == MASK_CAUSAL,
+                                               window=window, n_splits=ns)
+            torch.cuda.synchronize()
+            ro, rlse = attention_paged(q.double().numpy(), kc.double().numpy(), vc.double().numpy(), table, sl, ps,
+                                       0.1, mk, wl, wr)
+            o = o.float().cpu().numpy().astype(np.float64)
+            lse = lse.cpu().numpy().astype(np.float64)
+            what = f"paged {dtype} H={H} Hkv={Hkv} Nq={Nq} ps={ps} mask={mk} splits={ns}"
+            live = np.isfinite(rlse)
+            assert np.array_equal(np.isfinite(lse), live), what
+            err = np.abs(o - ro)
+            if dtype == "f32":
+                assert err.max() <= 1e-5, what
+            else:
+                assert (err - _half_ulp(ro, dtype)).max() <= 5e-5, what
+            assert np.abs(lse[live] - rlse[live]).max() <= 1e-5, what
+
+
+def test_paged_in_order_equals_contiguous_decode():
+    B, H, Hkv, Nq, Nk, D, ps = 2, 8, 2, 1, 4096, 128, 256
+    q, _, _ = make_qkv(B, H, Nq, D, "bf16", seed=31, n_k=1)
+    _, k, v = make_qkv(B, Hkv, 1, D, "bf16", seed=32, n_k=Nk)
+    kb, vb = (t.permute(0, 2, 1, 3).contiguous() for t in (k, v))   # [B, Nk, Hkv, D]
+    kc = kb.reshape(B * (Nk // ps), ps, Hkv, D).contiguous()
+    vc = vb.reshape(B * (Nk // ps), ps, Hkv, D).contiguous()
+    table = torch.arange(B * (Nk // ps), dtype=torch.int32).reshape(B, Nk // ps)
+    sl = torch.full((B,), Nk, dtype=torch.int32)
+    qc = q.cuda()
+    o1, l1 = fa.attention_decode_paged(qc, kc.cuda(), vc.cuda(), table.cuda(), sl.cuda(), causal=True)
+    o2, l2 = fa.attention_decode(qc.permute(0, 2, 1, 3).contiguous(), kb.cuda(), vb.cuda(), causal=True,
+                                 layout="bnhd")
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2.permute(0, 2, 1, 3)) and torch.equal(l1, l2)
+
+
+def test_paged_short_sequences_see_no_key():
+    # a sequence shorter than its query count: its early queries sit at negative positions
+    q, kc, vc, table, sl = _paged_case(2, 4, 4, 3, [1, 50], 64, 16, "f16", seed=40)
+    o, lse = fa.attention_decode_paged(q.cuda(), kc.cuda(), vc.cuda(), torch.from_numpy(table).cuda(),
+                                       torch.from_numpy(sl).cuda(), causal=True)
+    torch.cuda.synchronize()
+    lse = lse.cpu()
+    assert torch.isinf(lse[0, :, :2]).all() and torch.isfinite(lse[0, :, 2]).all() and torch.isfinite(lse[1]).all()
+    assert (o.cpu()[0, :, :2] == 0).all()

@@ -248,3 +248,23 @@ def test_rope_tables_validation(lib, kw, code):
     a = dict(cos=16, sin=32, n_pos=4, D=8, base=10000.0)
     a.update(kw)
     assert lib.fa_rope_tables(a["cos"], a["sin"], a["n_pos"], a["D"], a["base"], None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), fb.FA_ERR_ARG),
+    (dict(ps=24), fb.FA_ERR_ARG),              # not a power of two
+    (dict(max_pages=1), fb.FA_ERR_ARG),        # 1 x 16 < max_seq_len 64
+    (dict(num_pages=0), fb.FA_ERR_ARG),
+    (dict(Hkv=3), fb.FA_ERR_ARG),
+    (dict(D=96), fb.FA_ERR_UNSUPPORTED),
+    (dict(table=18), fb.FA_ERR_ALIGN),
+    (dict(k=24), fb.FA_ERR_ALIGN),
+])
+def test_paged_decode_validation(lib, kw, code):
+    a = dict(q=16, k=32, v=48, table=64, lens=80, o=96, B=1, H=2, Hkv=1, Nq=1, max_seq=64, ps=16, max_pages=4,
+             num_pages=8, D=64, dt=0)
+    a.update(kw)
+    rc = lib.fa_decode_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["o"], None, a["B"], a["H"], a["Hkv"],
+                             a["Nq"], a["max_seq"], a["ps"], a["max_pages"], a["num_pages"], a["D"], 0.1, 0, -1, -1,
+                             a["dt"], 0, 0, None, 0, None)
+    assert rc == code
