@@ -60,28 +60,6 @@ struct Waiter {
         bool ok = wait(bar, parity);
         return __all_sync(0xffffffffu, ok);
     }
-    // Bounded wait that lets the hardware suspend the thread between probes
-    // (for warps whose waits are long and whose issue slots another thread on
-    // the same sub-partition needs).
-    __device__ __forceinline__ bool wait_sleep(uint32_t bar, uint32_t parity) const {
-        if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(bar, parity)) return true;
-            if ((it & 3u) == 0) {
-                if (*abort) return false;
-                if (globaltimer_ns() - t0 > limit) {
-                    *abort = 1;
-                    atomicExch(status, DEV_TIMEOUT);
-                    return false;
-                }
-            }
-        }
-    }
-    __device__ __forceinline__ bool wait_warp_sleep(uint32_t bar, uint32_t parity) const {
-        bool ok = wait_sleep(bar, parity);
-        return __all_sync(0xffffffffu, ok);
-    }
     // Bounded wait that ignores the abort flag: lets in-flight async work land
     // before the CTA releases its resources.
     __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
