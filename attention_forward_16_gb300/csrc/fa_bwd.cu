@@ -41,11 +41,13 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kParts = 2;                     // column parts of a tile row, one warp each
+constexpr int kColsPerPart = 128 / kParts;
+constexpr int kBwdThreads = 128 + 128 * kParts;
 constexpr int kWarpTmaB = 0;
 constexpr int kWarpMmaB = 1;
-constexpr int kWarpEw0 = 4;  // first of the eight elementwise warps (4 .. 11)
-constexpr int kEwThreads = 256;
+constexpr int kWarpEw0 = 4;  // first of the 4 * kParts elementwise warps
+constexpr int kEwThreads = 128 * kParts;
 constexpr float kLog2e = 1.4426950408889634074f;
 
 template <int D>
@@ -115,12 +117,15 @@ struct Mma {
         }
     }
     // dst[128 x D] (+)= T[128 x 128] B[128 x D]: T 16-bit in TMEM, its K
-    // columns [64 h, 64 h + 64) packed at TMEM column t + 64 h (32 columns).
+    // columns of part c, [c P, c P + P) with P = kColsPerPart, packed at TMEM
+    // column t + c P (P / 2 columns).
     static __device__ __forceinline__ void cols(uint32_t dst, uint32_t t, uint32_t b, bool acc) {
+        constexpr int kSteps = kColsPerPart / 16;  // K-steps of 16 per part
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
             const uint64_t bd = make_sdesc(b + kk * 2048, BwdCfg<D>::kBoxBytes, 1024);
-            mma_ts(dst, t + (kk / 4) * 64 + (kk % 4) * 8, bd, kIdescCols, (acc || kk > 0) ? 1u : 0u);
+            mma_ts(dst, t + (kk / kSteps) * kColsPerPart + (kk % kSteps) * 8, bd, kIdescCols,
+                   (acc || kk > 0) ? 1u : 0u);
         }
     }
 };
@@ -157,19 +162,21 @@ __device__ __forceinline__ float4 lds_f4(const void* p) {
     return r;
 }
 
-// A thread's 64-column half row of fp32 values from TMEM into registers.
-__device__ __forceinline__ void ld_half(uint32_t t, uint32_t (&r)[2][32]) {
-    tmem_ld32(t, r[0]);
-    tmem_ld32(t + 32, r[1]);
+constexpr int kChunks = kColsPerPart / 32;  // 32-column TMEM loads per part
+
+// A thread's part of a row (kColsPerPart fp32 values) from TMEM into registers.
+__device__ __forceinline__ void ld_part(uint32_t t, uint32_t (&r)[kChunks][32]) {
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) tmem_ld32(t + 32 * c, r[c]);
     tmem_wait_ld();
 }
 
-// Store half `hf` of the columns of a thread's row of a 16-bit gradient
-// (fp32 in TMEM, times `mul`).
+// Store part `pt`'s 32-column chunks (pt, pt + kParts, ...) of a thread's row
+// of a 16-bit gradient (fp32 in TMEM, times `mul`).
 template <int D, bool kBf16>
-__device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, int hf, float mul, bool live) {
+__device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, int pt, float mul, bool live) {
 #pragma unroll 1
-    for (int c = hf * (D / 64); c < (hf + 1) * (D / 64); ++c) {
+    for (int c = pt; c < D / 32; c += kParts) {
         uint32_t v[32];
         tmem_ld32(t + c * 32, v);
         tmem_wait_ld();
@@ -186,10 +193,12 @@ __device__ __forceinline__ void store_row(uint32_t t, void* out, size_t row, int
 }
 
 template <int D>
-__device__ __forceinline__ void zero_row(void* out, size_t row, int hf) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D + hf * (D / 2));
+__device__ __forceinline__ void zero_row(void* out, size_t row, int pt) {
+    for (int c = pt; c < D / 32; c += kParts) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + row * D + c * 32);
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+    }
 }
 
 // ===================================================================== dK, dV
@@ -298,31 +307,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------- P, dS, epilogue
         const int wq = (warp - kWarpEw0) & 3;   // TMEM lane quarter
-        const int hf = (warp - kWarpEw0) >> 2;  // query-column half of the tile
+        const int hf = (warp - kWarpEw0) >> 2;  // query-column part of the tile
         const int c = wq * 32 + lane;           // key row within the tile
         const int kc = j * kTileN + c;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS + hf * 64;
-        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * 64;
+        const uint32_t tS = tmem + lane_base + C::kColS + hf * kColsPerPart;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * kColsPerPart;
         const float c2 = p.scale_log2;
         bool ok = true;
         for (int n = 0; n < n_items && ok; ++n) {
             int h, i;
             item(n, h, i);
             const uint8_t* stage = smem + 2 * C::kTileBytes + (n % C::kStages) * C::kStageKV;
-            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes) + hf * 16;
-            const float4* dsum = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * 16;
+            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes) + hf * (kColsPerPart / 4);
+            const float4* dsum =
+                reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * (kColsPerPart / 4);
             if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1))) break;
             if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
             tc_fence_after();
-            uint32_t s[2][32];
-            ld_half(tS, s);
+            uint32_t s[kChunks][32];
+            ld_part(tS, s);
             const bool masked = tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
             int r_lo = 0, r_hi = kTileM - 1;
             if (masked) key_visible_rows(p.g, kc, i, r_lo, r_hi);
             // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < kChunks; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
                     e2 = ex2(e2);
                     e3 = ex2(e3);
                     if (masked) {
-                        const int q = hf * 64 + cc * 32 + 4 * v;
+                        const int q = hf * kColsPerPart + cc * 32 + 4 * v;
                         if (q < r_lo || q > r_hi) e0 = 0.f;
                         if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
                         if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
@@ -356,10 +366,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             // dS^T: p * (dP - Dsum_q), written over dP columns of this half already read
             if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
             tc_fence_after();
-            uint32_t d[2][32];
-            ld_half(tDP, d);
+            uint32_t d[kChunks][32];
+            ld_part(tDP, d);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < kChunks; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) {
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->ds_full));
         }
-        // epilogue: this half's columns of dV and scale * dK for the keys that exist
+        // epilogue: this part's columns of dV and scale * dK for the keys that exist
         const bool live = kc < p.g.N;
         const size_t row = (size_t)row_index(p.layout, b, hk, live ? kc : 0, p.Hkv, p.g.N);
         if (n_items == 0) {
@@ -493,12 +503,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------------- dS, epilogue
         const int wq = (warp - kWarpEw0) & 3;   // TMEM lane quarter
-        const int hf = (warp - kWarpEw0) >> 2;  // key-column half of the tile
+        const int hf = (warp - kWarpEw0) >> 2;  // key-column part of the tile
         const int row = wq * 32 + lane;
         const int qi = r0 + row;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::kColS + hf * 64;
-        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * 64;
+        const uint32_t tS = tmem + lane_base + C::kColS + hf * kColsPerPart;
+        const uint32_t tDP = tmem + lane_base + C::kColDP + hf * kColsPerPart;
         const size_t vrow = (size_t)bh * p.Npad + qi;
         const float lse2 = p.lse2[vrow];
         const float dsum = p.dsum[vrow];
@@ -508,15 +518,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             const int j = jlo + n;
             if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
             tc_fence_after();
-            uint32_t s[2][32];
-            ld_half(tS, s);
+            uint32_t s[kChunks][32];
+            ld_part(tS, s);
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->s_free));
             const bool masked = tile_needs_mask(p.g, r0, j);  // uniform over the CTA
             int c_lo = 0, c_hi = kTileN - 1;
             if (masked) row_visible_cols(p.g, qi, j, c_lo, c_hi);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
+            for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
                 for (int v = 0; v < 32; v += 2) {
                     float e0, e1;
@@ -524,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
                     e0 = ex2(e0);
                     e1 = ex2(e1);
                     if (masked) {
-                        const int col = hf * 64 + cc * 32 + v;
+                        const int col = hf * kColsPerPart + cc * 32 + v;
                         if (col < c_lo || col > c_hi) e0 = 0.f;
                         if (col + 1 < c_lo || col + 1 > c_hi) e1 = 0.f;
                     }
@@ -533,10 +543,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
                 }
             if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
             tc_fence_after();
-            uint32_t d[2][32];
-            ld_half(tDP, d);
+            uint32_t d[kChunks][32];
+            ld_part(tDP, d);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < kChunks; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int v = 0; v < 16; ++v) {
