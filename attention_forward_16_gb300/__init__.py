@@ -1,9 +1,13 @@
-"""GB300-native (sm_103a) fused attention forward.
+"""GB300-native (sm_103a) fused attention.
 
 ``attention_fwd(q, k, v, scale=None, causal=False, window=None)`` returns
-(O, LSE) for contiguous [B, H, N, D] CUDA tensors, computed by libfa's
-hand-written tcgen05/TMA kernels (fp16 / bf16) or its fp32 FFMA kernel.
-The C ABI is declared in ``include/fa.h``; ``binding`` mirrors it.
+(O, LSE) for contiguous [B, H, N, D] (or [B, N, H, D]) CUDA tensors, computed
+by libfa's hand-written tcgen05/TMA kernels (fp16 / bf16) or its fp32 FFMA
+kernel.  Around it: ``attention_decode`` / ``attention_decode_paged`` (split-K
+decode against a contiguous or paged K/V cache), ``attention_bwd`` (dQ, dK,
+dV), ``apply_rope`` / ``rope_tables`` / ``attention_fwd_rope`` (rotary
+embedding of Q and K).  The C ABI is declared in ``include/fa.h``;
+``binding`` mirrors it, and a missing library raises.
 """
 
 from .binding import (  # noqa: F401

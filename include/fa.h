@@ -21,8 +21,11 @@
  * ({B, H, S, D} ND tensors).  LSE is a contiguous [B, H, N] fp32 tensor.
  *
  * Ownership: every pointer is caller-owned CUDA device memory; the library
- * allocates nothing and keeps no reference after the kernel finishes.
- * Pointers must be 16-byte aligned.  O must not alias Q, K or V.
+ * allocates nothing and keeps no reference after the kernel finishes (the
+ * decode and backward entry points take a caller workspace sized by their
+ * planning calls).  Pointers must be 16-byte aligned.  O must not alias Q, K
+ * or V.  The later sections declare the decode, layout / grouped-head,
+ * backward and rotary-embedding entry points, each with its own layouts.
  *
  * Asynchrony: a return of FA_OK means the work was enqueued on `stream`
  * (a cudaStream_t, or 0 for the legacy default stream).  Kernel-side
