@@ -44,7 +44,7 @@ from .attention import (  # noqa: F401
     attention_bruteforce,
     unmasked_pairs,
 )
-from .backward import attention_backward, attention_backward_grouped  # noqa: F401
+from .backward import attention_backward, attention_backward_grouped, attention_backward_sampled  # noqa: F401
 from .paged import attention_paged, gather_pages  # noqa: F401
 from .rope import (  # noqa: F401
     STYLE_HALF,

@@ -59,3 +59,32 @@ def attention_backward_grouped(q, k, v, do, scale, mask_kind=MASK_NONE, win_l=-1
     dk = dke.reshape(B, Hkv, g, Nk, D).sum(axis=2)
     dv = dve.reshape(B, Hkv, g, Nk, D).sum(axis=2)
     return dq, dk, dv
+
+
+def attention_backward_sampled(q, k, v, do, scale, mask_kind=MASK_NONE, win_l=-1, win_r=-1, rows=(), keys=(),
+                               row_chunk=1024):
+    """dQ for the query rows `rows` and dK, dV for the keys `keys` of ONE (batch,
+    head) ([N, D] arrays), by the same chain rule, for sequences too long for the
+    whole N x N probability matrix: P's rows are formed a chunk at a time with
+    the row max and sum of the definition, and only the requested rows and
+    columns of dS are kept.  Returns (dq [len(rows), D], dk, dv [len(keys), D])."""
+    from .attention import allowed_mask
+    q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
+    n = q.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    keys = np.asarray(keys, dtype=np.int64)
+    dq = np.zeros((len(rows), q.shape[1]))
+    dk = np.zeros((len(keys), k.shape[1]))
+    dv = np.zeros((len(keys), v.shape[1]))
+    for c0 in range(0, n, row_chunk):
+        c1 = min(n, c0 + row_chunk)
+        p = attention_probs(q[c0:c1], k, scale, mask_kind, win_l, win_r, q_offset=c0)   # [chunk, Nk]
+        dp = do[c0:c1] @ v.T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        if len(keys):
+            dv += p[:, keys].T @ do[c0:c1]
+            dk += scale * (ds[:, keys].T @ q[c0:c1])
+        sel = (rows >= c0) & (rows < c1)
+        if sel.any():
+            dq[sel] = scale * (ds[rows[sel] - c0] @ k)
+    return dq, dk, dv

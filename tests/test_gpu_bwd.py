@@ -183,3 +183,51 @@ def test_backward_full_size_sampled_heads(dtype, mk):
         _check(_f64(gv[sl]), rv, bv, dtype, f"dV full ({b},{h})")
         _check(_f64(gk[sl]), rk, bk, dtype, f"dK full ({b},{h})")
         _check(_f64(gq[sl]), rq, bq, dtype, f"dQ full ({b},{h})")
+
+
+def _sampled_bounds(q, k, v, do, o16, scale, mk, wl, wr, dtype, rows, keys, chunk=1024):
+    """The module's per-entry bounds for sampled dQ rows and dK, dV keys of one
+    head ([N, D] float64 arrays), formed a chunk of query rows at a time."""
+    from oracle import attention_probs
+    u = U[dtype]
+    rel = 1.05 * u + 2.0 ** -16
+    rows, keys = np.asarray(rows), np.asarray(keys)
+    bq = np.zeros((len(rows), q.shape[1]))
+    bk = np.zeros((len(keys), q.shape[1]))
+    bv = np.zeros((len(keys), q.shape[1]))
+    for c0 in range(0, q.shape[0], chunk):
+        c1 = min(q.shape[0], c0 + chunk)
+        p = attention_probs(q[c0:c1], k, scale, mk, wl, wr, q_offset=c0)
+        dp = do[c0:c1] @ v.T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dsum_err = (np.abs(do[c0:c1]) * _half_ulp(o16[c0:c1], dtype)).sum(axis=1) + 1e-6
+        pd = p * dsum_err[:, None]
+        bv += rel * (p[:, keys].T @ np.abs(do[c0:c1]))
+        bk += abs(scale) * (rel * (np.abs(ds[:, keys]).T @ np.abs(q[c0:c1])) + pd[:, keys].T @ np.abs(q[c0:c1]))
+        sel = (rows >= c0) & (rows < c1)
+        if sel.any():
+            r = rows[sel] - c0
+            bq[sel] = abs(scale) * (rel * (np.abs(ds[r]) @ np.abs(k)) + pd[r] @ np.abs(k))
+    return bq, bk, bv
+
+
+@pytest.mark.parametrize("dtype,N,mk,wl,wr", [("bf16", 16384, MASK_CAUSAL, -1, -1),
+                                              ("f16", 16384, MASK_WINDOW, 2048, 0)])
+def test_backward_long_sequences_sampled(dtype, N, mk, wl, wr):
+    """A long sequence: sampled query rows (dQ) and keys (dK, dV) against the
+    oracle's chunked backward, within the module's bound (the oracle forms
+    whole 16,384-key rows, seconds of host time per head)."""
+    from oracle import attention_backward_sampled
+    B, H, D = 1, 1, 128
+    q, k, v, do = _inputs(B, H, H, N, D, dtype, seed=N)
+    scale = 1.0 / math.sqrt(D)
+    gq, gk, gv, o16 = _run(q, k, v, do, mk, wl, wr)
+    rows = [0, 1, 4097, N // 2 + 3, N - 1]
+    keys = [0, 130, N // 2, N - 200, N - 1]
+    for h in range(H):
+        hq, hk, hv, hdo = (_f64(t[0, h]) for t in (q, k, v, do))
+        rq, rk, rv = attention_backward_sampled(hq, hk, hv, hdo, scale, mk, wl, wr, rows, keys)
+        bq, bk, bv = _sampled_bounds(hq, hk, hv, hdo, _f64(o16[0, h]), scale, mk, wl, wr, dtype, rows, keys)
+        _check(_f64(gq[0, h])[rows], rq, bq, dtype, f"dQ N={N} head {h}")
+        _check(_f64(gk[0, h])[keys], rk, bk, dtype, f"dK N={N} head {h}")
+        _check(_f64(gv[0, h])[keys], rv, bv, dtype, f"dV N={N} head {h}")

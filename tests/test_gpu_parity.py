@@ -397,3 +397,29 @@ def test_full_size_every_head(name):
                                             w.scale, w.mask, w.win_l, w.win_r)
             _check(o[b:b + 1, h:h + 1].astype(np.float64), lse[b:b + 1, h:h + 1].astype(np.float64), ro, rlse,
                    w.dtype, False, f"{name} head {(b, h)}")
+
+
+@pytest.mark.parametrize("dtype,D,N,mk,wl,wr", [
+    ("bf16", 128, 65536, MASK_CAUSAL, -1, -1),
+    ("f16", 128, 65536, MASK_WINDOW, 4096, 0),
+    ("f16", 64, 32768, MASK_NONE, -1, -1),
+])
+def test_long_sequences_sampled_rows(dtype, D, N, mk, wl, wr):
+    """Long sequences (row and tile indices far past 2^16): the first, last and
+    strided rows of two heads against the oracle computed row block by row block."""
+    B, H = 1, 2
+    q, k, v = make_qkv(B, H, N, D, dtype, seed=N + D)
+    scale = 1.0 / math.sqrt(D)
+    window = (wl, wr) if mk == MASK_WINDOW else None
+    o, lse = fa.attention_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=mk == MASK_CAUSAL, window=window)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    for h in range(H):
+        for r0 in (0, 13 * 1021, N // 2 + 7, N - 64):
+            ro, rlse = attention_three_pass(qd[:, h:h + 1, r0:r0 + 64], kd[:, h:h + 1], vd[:, h:h + 1], scale, mk,
+                                            wl, wr, q_offset=r0)
+            _check(o[:, h:h + 1, r0:r0 + 64].astype(np.float64), lse[:, h:h + 1, r0:r0 + 64].astype(np.float64),
+                   ro, rlse, dtype, False, f"N={N} head {h} rows {r0}..")

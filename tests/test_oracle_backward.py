@@ -140,3 +140,17 @@ def test_planted_mistakes_fail_finite_differences(mistake):
     want = _finite_diff(q, k, v, g, scale, MASK_CAUSAL, -1, -1)
     got = _broken(q, k, v, g, scale, MASK_CAUSAL, -1, -1, 0, mistake)
     assert any(not np.allclose(a, b, atol=2e-7) for a, b in zip(got, want))
+
+
+@pytest.mark.parametrize("mk,wl,wr", MASKS)
+def test_sampled_backward_equals_full(mk, wl, wr):
+    from oracle import attention_backward_sampled
+    N, D = 70, 8
+    q, k, v, g = (_rand((1, 1, N, D), 50 + i) for i in range(4))
+    dq, dk, dv = attention_backward(q, k, v, g, 0.6, mk, wl, wr)
+    rows, keys = [0, 5, 33, 69], [1, 2, 40, 69]
+    sq, sk, sv = attention_backward_sampled(q[0, 0], k[0, 0], v[0, 0], g[0, 0], 0.6, mk, wl, wr, rows, keys,
+                                            row_chunk=16)
+    assert np.allclose(sq, dq[0, 0, rows], atol=1e-13)
+    assert np.allclose(sk, dk[0, 0, keys], atol=1e-13)
+    assert np.allclose(sv, dv[0, 0, keys], atol=1e-13)
