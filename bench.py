@@ -158,6 +158,9 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if args.impl == "native" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)  # bind this rank to its GPU before NCCL sees it
         dist.init_process_group(backend=backend)
         pg = dist
     return world, rank, local, pg
