@@ -13,9 +13,9 @@
 //
 //   warps 0-3   Q tile 0: softmax (thread = one query row), then its epilogue
 //   warps 4-7   Q tile 1: same
-//   warp  8     TMEM allocator; one thread issues Q tile 0's tcgen05.mma
+//   warp  8     TMEM allocator; issues Q tile 0's tcgen05.mma (one elected lane)
 //   warp  9     one thread issues every TMA load (Q tiles, K/V ring)
-//   warp  10    one thread issues Q tile 1's tcgen05.mma
+//   warp  10    issues Q tile 1's tcgen05.mma (one elected lane)
 //   warp  11    idle (completes the third warpgroup)
 //
 // The launch gives 168 registers a thread (12 warps, three per SM
@@ -27,8 +27,8 @@
 // overwrites the first half of its S columns and feeds the P.V MMA straight
 // from TMEM.  The two softmax warpgroups ping-pong: while one turns S into P,
 // the tensor core runs the other tile's MMAs.  Each tile has its own issuing
-// thread (order P.V(j), S(j+1) per tile), so the two tiles settle into
-// alternating on the tensor core without waiting for each other.
+// warp (order P.V(j), S(j+1) per tile), and the two take turns on the tensor
+// core.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records a
 // timeout in the device status word, lets its in-flight copies and MMAs
@@ -146,13 +146,22 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
 }
 
 // -------------------------------------------------------------- MMA issuers
-// One issuing thread per Q tile t: S_t(j) = Q_t K_j^T and O_t += P_t(j) V_j.
-// Each thread keeps its own tile's order (S_t(j+1) after P.V_t(j), since P
-// aliases S); the two threads run independently, so one tile's slow softmax
-// never delays the other tile's MMAs.  A K/V ring slot and the Q buffer are
-// released once both threads have arrived (count 2); a tile with no work on
-// key tile j still waits for that slot to be full before arriving, which
-// keeps the phases of the ring aligned.
+// One issuing warp per Q tile t: S_t(j) = Q_t K_j^T and O_t += P_t(j) V_j.
+// Each warp keeps its own tile's order (S_t(j+1) after P.V_t(j), since P
+// aliases S).  A K/V ring slot and the Q buffer are released once both warps
+// have arrived (count 2); a tile with no work on key tile j still waits for
+// that slot to be full before arriving, which keeps the phases of the ring
+// aligned.
+//
+// The whole warp runs this role on one path: every wait, counter and shared-
+// memory descriptor is warp-uniform, and one elected lane issues the
+// tcgen05.mma / commit instructions and the single mbarrier arrivals.  Issue
+// from a lone lane of a diverged warp ran at about 100 cycles per MMA, slower
+// than the tensor core's 64 cycles for a 128x128x16 product; from a converged
+// warp the tensor core stays fed.  Descriptors are formed once and advanced
+// by adding encoded offsets (the start address field holds address / 16, and
+// every shared address here stays below 256 KiB, so the add never carries out
+// of the field).
 template <int D, bool kBf16>
 __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
                                          uint32_t sKVa, uint32_t tmem, int t) {
@@ -168,76 +177,89 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
     const uint32_t q_full = smem_u32(&sh->q_full);
     const uint32_t q_empty = smem_u32(&sh->q_empty);
+    const bool leader = elect_one();
     uint32_t kv_it = 0, q_it = 0, p_cnt = 0, o_cnt = 0;
     bool ok = true;
     volatile unsigned long long* my_progress = &sh->progress[t];
     volatile unsigned long long* other_progress = &sh->progress[1 - t];
     // The two issuers alternate on the tensor core: tile 1 issues key step j
     // only after tile 0 has, and tile 0 issues step j only after tile 1 has
-    // issued step j - 1.  Each thread still wakes on its own P, so neither
+    // issued step j - 1.  Each warp still wakes on its own P, so neither
     // tile's P waits behind the other tile's MMA issue, and the two softmaxes
     // stay half a step apart instead of competing for the same cycles.
-    auto publish = [&](unsigned long long v) { *my_progress = v; };
+    auto publish = [&](unsigned long long v) {
+        if (leader) *my_progress = v;
+    };
     auto wait_turn = [&](unsigned long long target) {
-        if (*other_progress >= target) return true;
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-            if (*other_progress >= target) return true;
-            if ((it & 15u) == 0) {
-                if (*W.abort) return false;
-                if (globaltimer_ns() - t0 > W.limit) {
-                    *W.abort = 1;
-                    atomicExch(W.status, DEV_TIMEOUT);
-                    return false;
+        bool r = true;
+        if (*other_progress < target) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it = 1;; ++it) {
+                if (*other_progress >= target) break;
+                if ((it & 15u) == 0) {
+                    if (*W.abort) {
+                        r = false;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > W.limit) {
+                        *W.abort = 1;
+                        atomicExch(W.status, DEV_TIMEOUT);
+                        r = false;
+                        break;
+                    }
                 }
             }
         }
+        return __all_sync(0xffffffffu, r);
     };
 
     // S = Q K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
+    const uint64_t q_desc = make_sdesc(qa, 16, 1024);
+    const uint64_t k_desc = make_sdesc(sKVa, 16, 1024);
+    const uint64_t v_desc = make_sdesc(sKVa, C::kBoxBytes, 1024);
     auto issue_s = [&](uint32_t slot) {
+        const uint64_t kb = k_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            const uint64_t a = make_sdesc(qa + off, 16, 1024);
-            const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + off, 16, 1024);
-            mma_ss(dS, a, b, idesc_s, kk > 0);
+            const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+            if (leader) mma_ss(dS, q_desc + off, kb + off, idesc_s, kk > 0);
         }
-        mma_commit(s_full);
+        if (leader) mma_commit(s_full);
     };
     // O += P V: P from TMEM (8 columns = 16 keys per step), V MN-major in
     // shared memory (16 keys = two 8-row swizzle atoms = 2048 bytes per step;
     // the second 64-column chunk of V sits one box further on).  With a split
     // P the low halves (64 columns further on) add a second product.
     auto issue_pv = [&](uint32_t slot, bool first, bool split) {
+        const uint64_t vb = v_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
-            mma_ts(dO, dS + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+            const uint64_t b = vb + (uint64_t)(kk * (2048 >> 4));
+            if (leader) mma_ts(dO, dS + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
         }
         if (split) {
 #pragma unroll
             for (int kk = 0; kk < kTileN / 16; ++kk) {
-                const uint64_t b = make_sdesc(sKVa + slot * C::kTileBytes + kk * 2048, C::kBoxBytes, 1024);
-                mma_ts(dO, dS + 64 + kk * 8, b, idesc_o, 1u);
+                const uint64_t b = vb + (uint64_t)(kk * (2048 >> 4));
+                if (leader) mma_ts(dO, dS + 64 + kk * 8, b, idesc_o, 1u);
             }
         }
     };
     auto wait_kv = [&](uint32_t idx) {
-        const bool r = W.wait(smem_u32(&sh->kv_full[idx % C::kStages]), (idx / C::kStages) & 1);
+        const bool r = W.wait_warp(smem_u32(&sh->kv_full[idx % C::kStages]), (idx / C::kStages) & 1);
         tc_fence_after();
         return r;
     };
     // Give back a slot this tile does not read.
     auto skip_kv = [&](uint32_t idx) {
         if (!wait_kv(idx)) return false;
-        mbar_arrive(smem_u32(&sh->kv_empty[idx % C::kStages]));
+        if (leader) mbar_arrive(smem_u32(&sh->kv_empty[idx % C::kStages]));
         return true;
     };
 
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
-        if (!(ok = W.wait(q_full, q_it & 1))) break;
+        if (!(ok = W.wait_warp(q_full, q_it & 1))) break;
         ++q_it;
         tc_fence_after();
         const uint32_t kbase = kv_it;  // ring index of K_jlo; V_j follows K_j
@@ -249,7 +271,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         auto kidx = [&](int j) { return kbase + 2 * (uint32_t)(j - un.jlo); };
         if (lo == hi) {
             publish(useq | 0xFFFFFFFFull);
-            mbar_arrive(q_empty);
+            if (leader) mbar_arrive(q_empty);
             for (int j = un.jlo; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
             continue;
         }
@@ -257,28 +279,32 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         for (int j = un.jlo; j < lo && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
         if (!ok || !(ok = wait_kv(kidx(lo)))) break;
         issue_s(kidx(lo) % C::kStages);
-        mma_commit(smem_u32(&sh->kv_empty[kidx(lo) % C::kStages]));
+        if (leader) mma_commit(smem_u32(&sh->kv_empty[kidx(lo) % C::kStages]));
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t v = kidx(j) + 1;
-            if (j == hi - 1) mma_commit(q_empty);  // this tile's last S is issued
+            if (j == hi - 1 && leader) mma_commit(q_empty);  // this tile's last S is issued
+            // V_j, and K_(j+1) for the S issued right after P.V_j, are waited
+            // for before P_j, so nothing stalls between the two MMA groups.
+            // K_(j+1) never waits on this step's P.V: its ring slot was freed
+            // by S(j-1) of both tiles, issued at least one step earlier.
             if (!(ok = wait_kv(v))) break;
-            if (!(ok = W.wait(p_full, p_cnt & 1))) break;
+            if (j + 1 < hi && !(ok = wait_kv(kidx(j + 1)))) break;
+            if (!(ok = W.wait_warp(p_full, p_cnt & 1))) break;
             ++p_cnt;
             const bool first = j == lo;
-            if (first && o_cnt > 0 && !(ok = W.wait(o_free, (o_cnt - 1) & 1))) break;
+            if (first && o_cnt > 0 && !(ok = W.wait_warp(o_free, (o_cnt - 1) & 1))) break;
             if (t == 1 && lo0 < hi0 && !(ok = wait_turn(useq | (unsigned long long)(j + 1 < hi0 ? j + 1 : hi0)))) break;
             if (t == 0 && j - 1 >= lo1 && j - 1 < hi1 && !(ok = wait_turn(useq | (unsigned long long)j))) break;
             tc_fence_after();
             issue_pv(v % C::kStages, first, split);
-            mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
+            if (leader) mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
             if (j == hi - 1) {
-                mma_commit(o_done);
+                if (leader) mma_commit(o_done);
                 ++o_cnt;
             } else {
                 const uint32_t k = kidx(j + 1);
-                if (!(ok = wait_kv(k))) break;
                 issue_s(k % C::kStages);
-                mma_commit(smem_u32(&sh->kv_empty[k % C::kStages]));
+                if (leader) mma_commit(smem_u32(&sh->kv_empty[k % C::kStages]));
             }
             publish(useq | (unsigned long long)(j + 1));
         }
@@ -286,7 +312,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     }
     // Every issued MMA must complete before TMEM is released.
     const uint32_t drain = smem_u32(&sh->drain[t]);
-    mma_commit(drain);
+    if (leader) mma_commit(drain);
     W.drain(drain, 0);
 }
 
@@ -487,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
     const uint32_t sQa = smem_u32(smem);
     const uint32_t sKVa = sQa + 2 * C::kTileBytes;
 
-    const int warp = threadIdx.x >> 5;
+    // Warp index through a shuffle, so the compiler sees it as warp-uniform.
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -518,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, sh->tmem_base, 0);
     const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
 
     // setmaxnreg is warpgroup-wide: all four warps of a group run the same one.
@@ -530,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
     if (warp < 8) {
         softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, warp, lane);
     } else if (warp == kWarpMma || warp == kWarpMma1) {
-        if (lane == 0) mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
+        mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
     } else if (warp == kWarpTma) {
         if (lane == 0) tma_role<D>(p, W, sh, sQa, sKVa);
     }
