@@ -109,23 +109,28 @@ struct Mma {
     static constexpr uint32_t kIdescRows = make_idesc(kBf16, kTileM, kTileN, false);  // 128 x 128, K = D
     static constexpr uint32_t kIdescCols = make_idesc(kBf16, kTileM, D, true);         // 128 x D, K = 128
     // dst[128 x 128] = A[128 x D] B[128 x D]^T, both from shared memory.
-    static __device__ __forceinline__ void rows(uint32_t dst, uint32_t a, uint32_t b) {
+    // Called by the whole issuing warp; `leader` (one elected lane) issues.
+    // Descriptors advance by encoded offsets (address / 16 in the low field;
+    // shared addresses stay below 256 KiB, so the add never leaves the field).
+    static __device__ __forceinline__ void rows(uint32_t dst, uint32_t a, uint32_t b, bool leader) {
+        const uint64_t ad = make_sdesc(a, 16, 1024), bd = make_sdesc(b, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * BwdCfg<D>::kBoxBytes + (kk % 4) * 32;
-            mma_ss(dst, make_sdesc(a + off, 16, 1024), make_sdesc(b + off, 16, 1024), kIdescRows, kk > 0);
+            const uint32_t off = ((kk / 4) * BwdCfg<D>::kBoxBytes + (kk % 4) * 32) >> 4;
+            if (leader) mma_ss(dst, ad + off, bd + off, kIdescRows, kk > 0);
         }
     }
     // dst[128 x D] (+)= T[128 x 128] B[128 x D]: T 16-bit in TMEM, its K
     // columns of part c, [c P, c P + P) with P = kColsPerPart, packed at TMEM
     // column t + c P (P / 2 columns).
-    static __device__ __forceinline__ void cols(uint32_t dst, uint32_t t, uint32_t b, bool acc) {
+    static __device__ __forceinline__ void cols(uint32_t dst, uint32_t t, uint32_t b, bool acc, bool leader) {
         constexpr int kSteps = kColsPerPart / 16;  // K-steps of 16 per part
+        const uint64_t bd = make_sdesc(b, BwdCfg<D>::kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t bd = make_sdesc(b + kk * 2048, BwdCfg<D>::kBoxBytes, 1024);
-            mma_ts(dst, t + (kk / kSteps) * kColsPerPart + (kk % kSteps) * 8, bd, kIdescCols,
-                   (acc || kk > 0) ? 1u : 0u);
+            if (leader)
+                mma_ts(dst, t + (kk / kSteps) * kColsPerPart + (kk % kSteps) * 8, bd + (uint64_t)(kk * (2048 >> 4)),
+                       kIdescCols, (acc || kk > 0) ? 1u : 0u);
         }
     }
 };
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     const uint32_t sV = sK + C::kTileBytes;
     const uint32_t sRing = sV + C::kTileBytes;
     BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + 2 * C::kTileBytes + C::kStages * C::kStageKV);
-    const int warp = threadIdx.x >> 5;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);  // warp-uniform to the compiler
     const int lane = threadIdx.x & 31;
 
     // CTA -> (b, K/V head, key tile j); consecutive CTAs share a head, so the
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, sh->tmem_base, 0);
     const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
     auto item = [&](int n, int& h, int& i) {
         h = hk * p.G + n / ni;
@@ -268,41 +273,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
         W.drain(fixed, 0);
         for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
             W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
-    } else if (warp == kWarpMmaB && lane == 0 && n_items > 0) {
+    } else if (warp == kWarpMmaB && n_items > 0) {
         // ------------------------------------------------------------ MMA
+        // The whole warp follows one path; the elected lane issues.
+        const bool leader = elect_one();
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
         const uint32_t tDV = tmem + C::kColA, tDK = tmem + C::kColB;
         auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageKV; };
-        auto ring_full = [&](int n) { return W.wait(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
-        bool ok = W.wait(smem_u32(&sh->fixed_full), 0) && ring_full(0);
+        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
+        bool ok = W.wait_warp(smem_u32(&sh->fixed_full), 0) && ring_full(0);
         if (ok) {
             tc_fence_after();
-            M::rows(tS, sK, stage(0));                       // S^T = K Q^T
-            mma_commit(smem_u32(&sh->s_full));
-            M::rows(tDP, sV, stage(0) + C::kTileBytes);      // dP^T = V dO^T
-            mma_commit(smem_u32(&sh->dp_full));
+            M::rows(tS, sK, stage(0), leader);                       // S^T = K Q^T
+            if (leader) mma_commit(smem_u32(&sh->s_full));
+            M::rows(tDP, sV, stage(0) + C::kTileBytes, leader);      // dP^T = V dO^T
+            if (leader) mma_commit(smem_u32(&sh->dp_full));
         }
         for (int n = 0; n < n_items && ok; ++n) {
-            if (!(ok = W.wait(smem_u32(&sh->p_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->p_full), n & 1))) break;
             tc_fence_after();
-            M::cols(tDV, tS, stage(n) + C::kTileBytes, n > 0);   // dV += P^T dO
+            M::cols(tDV, tS, stage(n) + C::kTileBytes, n > 0, leader);   // dV += P^T dO
             if (n + 1 < n_items) {
                 if (!(ok = ring_full(n + 1))) break;
                 tc_fence_after();
-                M::rows(tS, sK, stage(n + 1));
-                mma_commit(smem_u32(&sh->s_full));
+                M::rows(tS, sK, stage(n + 1), leader);
+                if (leader) mma_commit(smem_u32(&sh->s_full));
             }
-            if (!(ok = W.wait(smem_u32(&sh->ds_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full), n & 1))) break;
             tc_fence_after();
-            M::cols(tDK, tDP, stage(n), n > 0);                  // dK += dS^T Q
-            mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
+            M::cols(tDK, tDP, stage(n), n > 0, leader);                  // dK += dS^T Q
+            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
             if (n + 1 < n_items) {
-                M::rows(tDP, sV, stage(n + 1) + C::kTileBytes);
-                mma_commit(smem_u32(&sh->dp_full));
+                M::rows(tDP, sV, stage(n + 1) + C::kTileBytes, leader);
+                if (leader) mma_commit(smem_u32(&sh->dp_full));
             }
         }
-        mma_commit(smem_u32(&sh->acc_done));
-        mma_commit(smem_u32(&sh->drain));
+        if (leader) mma_commit(smem_u32(&sh->acc_done));
+        if (leader) mma_commit(smem_u32(&sh->drain));
         W.drain(smem_u32(&sh->drain), 0);
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------- P, dS, epilogue
@@ -422,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     const uint32_t sDO = sQ + C::kTileBytes;
     const uint32_t sRing = sDO + C::kTileBytes;
     BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + 2 * C::kTileBytes + C::kStages * C::kStageQ);
-    const int warp = threadIdx.x >> 5;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);  // warp-uniform to the compiler
     const int lane = threadIdx.x & 31;
 
     // CTA -> (b, head, query tile i); consecutive CTAs share a head's K/V
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, sh->tmem_base, 0);
     const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
 
     if (warp == kWarpTmaB && lane == 0 && n_items > 0) {
@@ -467,38 +474,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         W.drain(fixed, 0);
         for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
             W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
-    } else if (warp == kWarpMmaB && lane == 0 && n_items > 0) {
+    } else if (warp == kWarpMmaB && n_items > 0) {
         // ------------------------------------------------------------ MMA
+        // The whole warp follows one path; the elected lane issues.
+        const bool leader = elect_one();
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColA;
         auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageQ; };
-        auto ring_full = [&](int n) { return W.wait(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
-        bool ok = W.wait(smem_u32(&sh->fixed_full), 0) && ring_full(0);
+        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
+        bool ok = W.wait_warp(smem_u32(&sh->fixed_full), 0) && ring_full(0);
         if (ok) {
             tc_fence_after();
-            M::rows(tS, sQ, stage(0));                       // S = Q K^T
-            mma_commit(smem_u32(&sh->s_full));
-            M::rows(tDP, sDO, stage(0) + C::kTileBytes);     // dP = dO V^T
-            mma_commit(smem_u32(&sh->dp_full));
+            M::rows(tS, sQ, stage(0), leader);                       // S = Q K^T
+            if (leader) mma_commit(smem_u32(&sh->s_full));
+            M::rows(tDP, sDO, stage(0) + C::kTileBytes, leader);     // dP = dO V^T
+            if (leader) mma_commit(smem_u32(&sh->dp_full));
         }
         for (int n = 0; n < n_items && ok; ++n) {
             if (n + 1 < n_items) {
                 // the next S may overwrite S once its row loads are done
-                if (!(ok = W.wait(smem_u32(&sh->s_free), n & 1) && ring_full(n + 1))) break;
+                if (!(ok = W.wait_warp(smem_u32(&sh->s_free), n & 1) && ring_full(n + 1))) break;
                 tc_fence_after();
-                M::rows(tS, sQ, stage(n + 1));
-                mma_commit(smem_u32(&sh->s_full));
+                M::rows(tS, sQ, stage(n + 1), leader);
+                if (leader) mma_commit(smem_u32(&sh->s_full));
             }
-            if (!(ok = W.wait(smem_u32(&sh->ds_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full), n & 1))) break;
             tc_fence_after();
-            M::cols(tDQ, tDP, stage(n), n > 0);               // dQ += dS K
-            mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
+            M::cols(tDQ, tDP, stage(n), n > 0, leader);               // dQ += dS K
+            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
             if (n + 1 < n_items) {
-                M::rows(tDP, sDO, stage(n + 1) + C::kTileBytes);
-                mma_commit(smem_u32(&sh->dp_full));
+                M::rows(tDP, sDO, stage(n + 1) + C::kTileBytes, leader);
+                if (leader) mma_commit(smem_u32(&sh->dp_full));
             }
         }
-        mma_commit(smem_u32(&sh->acc_done));
-        mma_commit(smem_u32(&sh->drain));
+        if (leader) mma_commit(smem_u32(&sh->acc_done));
+        if (leader) mma_commit(smem_u32(&sh->drain));
         W.drain(smem_u32(&sh->drain), 0);
     } else if (warp >= kWarpEw0) {
         // ------------------------------------------------------- dS, epilogue
