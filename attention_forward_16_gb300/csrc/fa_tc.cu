@@ -283,18 +283,21 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t v = kidx(j) + 1;
             if (j == hi - 1 && leader) mma_commit(q_empty);  // this tile's last S is issued
-            // V_j, and K_(j+1) for the S issued right after P.V_j, are waited
-            // for before P_j, so nothing stalls between the two MMA groups.
-            // K_(j+1) never waits on this step's P.V: its ring slot was freed
-            // by S(j-1) of both tiles, issued at least one step earlier.
+            // Every other condition of this step is met before P_j is waited
+            // for, so the MMAs go out as soon as P_j lands: V_j; K_(j+1) for the
+            // S issued right after P.V_j (its ring slot was freed by S(j-1) of
+            // both tiles, issued at least one step earlier, so it never waits on
+            // this step); the O accumulator at a unit's first step (freed by the
+            // previous epilogue, which precedes this unit's first P); and the
+            // other tile's turn (which never depends on this tile's P_j).
             if (!(ok = wait_kv(v))) break;
             if (j + 1 < hi && !(ok = wait_kv(kidx(j + 1)))) break;
-            if (!(ok = W.wait_warp(p_full, p_cnt & 1))) break;
-            ++p_cnt;
             const bool first = j == lo;
             if (first && o_cnt > 0 && !(ok = W.wait_warp(o_free, (o_cnt - 1) & 1))) break;
             if (t == 1 && lo0 < hi0 && !(ok = wait_turn(useq | (unsigned long long)(j + 1 < hi0 ? j + 1 : hi0)))) break;
             if (t == 0 && j - 1 >= lo1 && j - 1 < hi1 && !(ok = wait_turn(useq | (unsigned long long)j))) break;
+            if (!(ok = W.wait_warp(p_full, p_cnt & 1))) break;
+            ++p_cnt;
             tc_fence_after();
             issue_pv(v % C::kStages, first, split);
             if (leader) mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
