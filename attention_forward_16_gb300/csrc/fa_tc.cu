@@ -90,6 +90,10 @@ constexpr int smem_bytes() {
 }
 
 static_assert(smem_bytes<128>() <= 227 * 1024, "shared memory budget (D=128)");
+// The MMA issuers wait for K(j+1) before P(j); that is deadlock-free only while
+// K(j+1)'s ring slot was last used by K(j-1) or earlier (at least two key steps
+// of K/V in the ring), whose S products both tiles issued a step before.
+static_assert(TcCfg<128>::kStages >= 4 && TcCfg<64>::kStages >= 4, "K/V ring too short for the issue order");
 static_assert(smem_bytes<64>() <= 227 * 1024, "shared memory budget (D=64)");
 
 // ------------------------------------------------------------- TMA producer
