@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <mutex>
 #include <type_traits>
@@ -376,10 +378,11 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
         }
     }
 
-    // Masks only matter if some query does not see the whole key chunk
-    // (decode's usual case, every cached key visible, skips the per-key test).
-    bool all_vis = true;
-    for (int i = 0; i < p.Nq; ++i) all_vis = all_vis && dec_visible(p, i, k0, len) && dec_visible(p, i, k1 - 1, len);
+    // Keys every query sees: [vis_lo, vis_hi], the intersection of the
+    // queries' bands (query i sits at len - Nq + i).  A block inside it skips
+    // the per-key test, so only blocks at a band's edge pay for the mask.
+    const long long vis_lo = p.win_l >= 0 ? (long long)len - 1 - p.win_l : LLONG_MIN;
+    const long long vis_hi = p.win_r >= 0 ? (long long)len - p.Nq + p.win_r : LLONG_MAX;
 
     // key u of a block for this lane group: base + u * KPW + grp, so one load
     // instruction of the warp reads KPW consecutive rows
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
             for (int r = 0; r < 4; ++r) sc[u][r] = __shfl_sync(0xffffffffu, own, grp * L + r * (L / 4));
         }
         if (base + kStride < k1) load_block(base + kStride);
-        const bool full_block = all_vis && base + kBlock <= k1;
+        const bool full_block = base >= vis_lo && (long long)base + kBlock - 1 <= vis_hi && base + kBlock <= k1;
         if (!full_block) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -578,7 +581,42 @@ cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename Kern>
+int resident_ctas(Kern kern, size_t smem) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecThreads, smem) != cudaSuccess) return 0;
+    return n;
+}
+
 }  // namespace
+
+int decode_ctas_per_sm(int rows, int D) {
+    // The 16-bit instantiations stand for every dtype: the split plan (and so
+    // the workspace size) must not depend on the element type.
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev][3][2];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const int cls = rows == 1 ? 0 : rows <= 4 ? 1 : 2;
+    const int di = D == 128 ? 1 : 0;
+    int n = cache[dev][cls][di].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    using T = __nv_bfloat16;
+    if (cls == 0)
+        n = di ? resident_ctas(fa_decode_split_kernel<T, 4, 1>, sizeof(float) * kDecWarps * 1 * (128 + 2))
+               : resident_ctas(fa_decode_split_kernel<T, 2, 1>, sizeof(float) * kDecWarps * 1 * (64 + 2));
+    else if (cls == 1)
+        n = di ? resident_ctas(fa_decode_rows_kernel<T, 128>, sizeof(float) * kDecWarps * 2 * 4 * (128 + 2))
+               : resident_ctas(fa_decode_rows_kernel<T, 64>, sizeof(float) * kDecWarps * 4 * 4 * (64 + 2));
+    else
+        n = di ? resident_ctas(fa_decode_split_kernel<T, 4, kDecodeMaxQ>,
+                               sizeof(float) * kDecWarps * kDecodeMaxQ * (128 + 2))
+               : resident_ctas(fa_decode_split_kernel<T, 2, kDecodeMaxQ>,
+                               sizeof(float) * kDecWarps * kDecodeMaxQ * (64 + 2));
+    if (n > 0) cache[dev][cls][di].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s) {
     const int dv = p.D / 32;

@@ -90,9 +90,28 @@ struct DecodeParams {
 };
 
 // Split count and key chunk for a decode problem (n_req <= 0: choose).
-inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk) {
-    long long s = n_req > 0 ? n_req : (8LL * sms + BH - 1) / BH;
+//
+// With ctas_per_sm > 0 (the decode kernel's resident CTAs per SM, so one wave
+// is ctas_per_sm * sms CTAs) the choice is the split count, at most two waves'
+// worth, whose last wave is fullest (ties to fewer splits).  With
+// ctas_per_sm == 0 it is the older rule of about eight CTAs per SM.
+inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk, int ctas_per_sm = 0) {
     const long long cap = (Nk + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
+    long long s = n_req > 0 ? n_req : (8LL * sms + BH - 1) / BH;
+    if (n_req <= 0 && ctas_per_sm > 0) {
+        const long long slots = (long long)ctas_per_sm * sms;
+        long long best = 1;
+        double best_eff = -1.0;
+        for (long long t = 1; t <= cap && BH * t <= 2 * slots; ++t) {
+            const long long waves = (BH * t + slots - 1) / slots;
+            const double eff = (double)(BH * t) / (double)(waves * slots);
+            if (eff > best_eff + 1e-9) {
+                best_eff = eff;
+                best = t;
+            }
+        }
+        s = best;
+    }
     if (n_req <= 0 && s > cap) s = cap;
     if (s > Nk) s = Nk;
     if (s > 1024) s = 1024;
@@ -155,6 +174,9 @@ struct RopeParams {
 
 // Launchers (return the CUDA error of the launch, if any).
 cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s);
+// Resident CTAs per SM of the decode kernel that `rows` query rows per (b, K/V
+// head) select, at head dimension D (0 if the runtime cannot say).
+int decode_ctas_per_sm(int rows, int D);
 cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s);
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B,
