@@ -460,6 +460,14 @@ def run_native(args, w, world, rank, local, pg):
     return 0
 
 
+def decode_kernel_name(rows, n_splits):
+    """The decode kernels a call runs: one query row per (b, K/V head) takes the
+    split kernel, two to four the lane-group rows kernel, more the 16-row split
+    kernel; a combine pass follows when the cache is split."""
+    main = "fa_decode_split_kernel" if rows == 1 or rows > 4 else "fa_decode_rows_kernel"
+    return main + (" + fa_decode_combine_kernel" if n_splits > 1 else "")
+
+
 def run_decode(args, w, world, rank, local, pg):
     """Decode against a K/V cache: HBM-bound, reported as achieved GB/s of the
     compulsory traffic (cache read once, Q read, O and LSE written)."""
@@ -527,7 +535,7 @@ def run_decode(args, w, world, rank, local, pg):
                    "n_splits": ns, "workspace_bytes": wb,
                    "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * Hkv * w.Nk * w.D * e >> 20)},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "traffic": None, "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+                     "traffic": None, "kernel": decode_kernel_name(w.H // Hkv * w.Nq, ns),
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "peak_source": src},
         "clocks": clk, "gpu_launches": args.steps * (2 if ns > 1 else 1),
     }
