@@ -465,6 +465,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if ((rc = make_map(&p.tm_do, d_o, bf16, layout, B, H, N, D)) != FA_OK) return rc;
     float* lse2 = static_cast<float*>(workspace);
     float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + vb);
+    p.q = q;
+    p.d_o = d_o;
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;

@@ -15,14 +15,16 @@
 //   dkdv  one CTA per (b, K/V head, 128-key tile): K and V stay in shared
 //         memory, the query tiles of every query head of the group stream
 //         through a TMA ring; TMEM holds S^T | dP^T | dV | dK;
-//   dq    one CTA per (b, head, 128-row query tile): Q and dO stay, K/V
-//         tiles stream; TMEM holds S | dP | dQ.
+//   dq    one CTA per (b, head, 128-row query tile): K/V tiles stream; the
+//         stationary Q and dO rows sit in TMEM beside S | dP | dQ, so S and dP
+//         are TS products that read only K and V from shared memory.
 // The dq kernel recomputes S and dP rather than adding partial dQ tiles with
 // atomics from the dkdv kernel: two more products per tile pair, in exchange
 // for a deterministic result and no read-modify-write traffic in L2.
 //
 // Warp roles in both kernels (384 threads): warp 0 issues TMA loads, warp 1
-// allocates TMEM and one of its threads issues tcgen05.mma, warps 4-11 turn
+// allocates TMEM and issues tcgen05.mma (the whole warp on one uniform path,
+// one elected lane issuing), warps 4-11 turn
 // scores into P and dS and write the result; warps 2-3 only take part in the
 // CTA barriers.  Warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (one
 // row per thread) and split the 128 columns of a tile: nothing in P or dS
@@ -57,6 +59,7 @@ struct BwdCfg {
     static constexpr int kTileBytes = kChunks * kBoxBytes;   // 128 rows x D
     static constexpr int kVecBytes = kTileM * 4;             // 128 fp32 per-row values
     static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr int kStagesQ = D == 128 ? 3 : 4;       // dq ring: Q and dO live in TMEM
     // dkdv ring stage: Q tile | dO tile | LSE*log2e | Dsum (a multiple of 1024 bytes)
     static constexpr int kStageKV = 2 * kTileBytes + 1024;
     // dq ring stage: K tile | V tile
@@ -65,11 +68,14 @@ struct BwdCfg {
     static constexpr int kColDP = 128;
     static constexpr int kColA = 256;       // dV (dkdv) or dQ (dq)
     static constexpr int kColB = 256 + D;   // dK (dkdv)
+    static constexpr int kColQ = 256 + D;   // dq: Q, 16-bit pairs (D / 2 columns)
+    static constexpr int kColDO = 256 + D + D / 2;  // dq: dO, likewise
     static constexpr int kTmemCols = 512;
 };
 
 struct __align__(16) BwdCtl {
     uint64_t fixed_full;
+    uint64_t qd_full;  // dq: Q and dO rows stored in TMEM (one arrival per elementwise thread)
     uint64_t ring_full[4], ring_empty[4];
     uint64_t s_full, s_free, dp_full, p_full, ds_full, acc_done, drain;
     uint32_t tmem_base;
@@ -82,8 +88,10 @@ constexpr int dkdv_smem_bytes() {
 }
 template <int D>
 constexpr int dq_smem_bytes() {
-    return 2 * BwdCfg<D>::kTileBytes + BwdCfg<D>::kStages * BwdCfg<D>::kStageQ + (int)sizeof(BwdCtl) + 1024;
+    return BwdCfg<D>::kStagesQ * BwdCfg<D>::kStageQ + (int)sizeof(BwdCtl) + 1024;
 }
+static_assert(BwdCfg<128>::kStagesQ <= 4 && BwdCfg<64>::kStagesQ <= 4, "ring barriers");
+static_assert(BwdCfg<128>::kColDO + 64 <= BwdCfg<128>::kTmemCols && BwdCfg<64>::kColDO + 32 <= 512, "TMEM (dq)");
 static_assert(dkdv_smem_bytes<128>() <= 227 * 1024 && dq_smem_bytes<128>() <= 227 * 1024, "smem (D=128)");
 static_assert(dkdv_smem_bytes<64>() <= 227 * 1024 && dq_smem_bytes<64>() <= 227 * 1024, "smem (D=64)");
 
@@ -137,6 +145,7 @@ struct Mma {
 
 __device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count) {
     mbar_init(smem_u32(&sh->fixed_full), 1);
+    mbar_init(smem_u32(&sh->qd_full), kEwThreads);
     for (int s = 0; s < 4; ++s) {
         mbar_init(smem_u32(&sh->ring_full[s]), 1);
         mbar_init(smem_u32(&sh->ring_empty[s]), ring_empty_count);
@@ -425,10 +434,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     using M = Mma<D, kBf16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sQ = smem_u32(smem);
-    const uint32_t sDO = sQ + C::kTileBytes;
-    const uint32_t sRing = sDO + C::kTileBytes;
-    BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + 2 * C::kTileBytes + C::kStages * C::kStageQ);
+    const uint32_t sRing = smem_u32(smem);
+    BwdCtl* sh = reinterpret_cast<BwdCtl*>(smem + C::kStagesQ * C::kStageQ);
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);  // warp-uniform to the compiler
     const int lane = threadIdx.x & 31;
 
@@ -456,37 +463,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         // ------------------------------------------------------------ TMA
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
-        const uint32_t fixed = smem_u32(&sh->fixed_full);
-        mbar_arrive_expect_tx(fixed, 2 * C::kTileBytes);
-        load_tile<D>(sQ, &p.tm_q, fixed, p.layout, b, h, r0);
-        load_tile<D>(sDO, &p.tm_do, fixed, p.layout, b, h, r0);
         bool ok = true;
         int n = 0;
         for (; n < n_items && ok; ++n) {
-            const int st = n % C::kStages;
-            if (n >= C::kStages && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((n / C::kStages) - 1) & 1))) break;
+            const int st = n % C::kStagesQ;
+            if (n >= C::kStagesQ && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((n / C::kStagesQ) - 1) & 1))) break;
             const uint32_t full = smem_u32(&sh->ring_full[st]);
             const uint32_t stage = sRing + st * C::kStageQ;
             mbar_arrive_expect_tx(full, 2 * C::kTileBytes);
             load_tile<D>(stage, &p.tm_k, full, p.layout, b, hk, (jlo + n) * kTileN);
             load_tile<D>(stage + C::kTileBytes, &p.tm_v, full, p.layout, b, hk, (jlo + n) * kTileN);
         }
-        W.drain(fixed, 0);
-        for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
-            W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
+        for (int m = n - C::kStagesQ < 0 ? 0 : n - C::kStagesQ; m < n; ++m)
+            W.drain(smem_u32(&sh->ring_full[m % C::kStagesQ]), (m / C::kStagesQ) & 1);
     } else if (warp == kWarpMmaB && n_items > 0) {
         // ------------------------------------------------------------ MMA
         // The whole warp follows one path; the elected lane issues.
         const bool leader = elect_one();
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColA;
-        auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageQ; };
-        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
-        bool ok = W.wait_warp(smem_u32(&sh->fixed_full), 0) && ring_full(0);
+        const uint32_t tQ = tmem + C::kColQ, tDO = tmem + C::kColDO;
+        auto stage = [&](int n) { return sRing + (n % C::kStagesQ) * C::kStageQ; };
+        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStagesQ]), (n / C::kStagesQ) & 1); };
+        // S = Q K^T and dP = dO V^T with the stationary A operand read from TMEM
+        // (TS products): only K and V come from shared memory.
+        auto rows_t = [&](uint32_t dst, uint32_t ta, uint32_t b) {
+            const uint64_t bd = make_sdesc(b, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+                if (leader) mma_ts(dst, ta + kk * 8, bd + off, M::kIdescRows, kk > 0);
+            }
+        };
+        bool ok = W.wait_warp(smem_u32(&sh->qd_full), 0) && ring_full(0);
         if (ok) {
             tc_fence_after();
-            M::rows(tS, sQ, stage(0), leader);                       // S = Q K^T
+            rows_t(tS, tQ, stage(0));                                // S = Q K^T
             if (leader) mma_commit(smem_u32(&sh->s_full));
-            M::rows(tDP, sDO, stage(0) + C::kTileBytes, leader);     // dP = dO V^T
+            rows_t(tDP, tDO, stage(0) + C::kTileBytes);              // dP = dO V^T
             if (leader) mma_commit(smem_u32(&sh->dp_full));
         }
         for (int n = 0; n < n_items && ok; ++n) {
@@ -494,15 +507,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
                 // the next S may overwrite S once its row loads are done
                 if (!(ok = W.wait_warp(smem_u32(&sh->s_free), n & 1) && ring_full(n + 1))) break;
                 tc_fence_after();
-                M::rows(tS, sQ, stage(n + 1), leader);
+                rows_t(tS, tQ, stage(n + 1));
                 if (leader) mma_commit(smem_u32(&sh->s_full));
             }
             if (!(ok = W.wait_warp(smem_u32(&sh->ds_full), n & 1))) break;
             tc_fence_after();
             M::cols(tDQ, tDP, stage(n), n > 0, leader);               // dQ += dS K
-            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
+            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStagesQ]));
             if (n + 1 < n_items) {
-                M::rows(tDP, sDO, stage(n + 1) + C::kTileBytes, leader);
+                rows_t(tDP, tDO, stage(n + 1) + C::kTileBytes);
                 if (leader) mma_commit(smem_u32(&sh->dp_full));
             }
         }
@@ -523,6 +536,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         const float dsum = p.dsum[vrow];
         const float c2 = p.scale_log2;
         bool ok = true;
+        if (n_items > 0) {
+            // This thread's row of Q and of dO, its half of the columns, into TMEM as
+            // 16-bit pairs (column c holds elements 2c and 2c + 1): the A operands of
+            // S = Q K^T and dP = dO V^T.  Rows past N are zeros.
+            const bool live_q = qi < p.g.N;
+            const size_t qrow = (size_t)row_index(p.layout, b, h, live_q ? qi : 0, p.H, p.g.N);
+            constexpr int kWords = D / 4;  // 32-bit words in half a row
+            const uint16_t* srcs[2] = {static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o)};
+            const uint32_t dsts[2] = {tmem + lane_base + C::kColQ + hf * kWords, tmem + lane_base + C::kColDO + hf * kWords};
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const uint4* src = reinterpret_cast<const uint4*>(srcs[x] + qrow * D + hf * (D / 2));
+#pragma unroll
+                for (int c = 0; c < kWords / 16; ++c) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 u = live_q ? src[c * 4 + v] : make_uint4(0, 0, 0, 0);
+                        w[4 * v] = u.x;
+                        w[4 * v + 1] = u.y;
+                        w[4 * v + 2] = u.z;
+                        w[4 * v + 3] = u.w;
+                    }
+                    tmem_st16(dsts[x] + 16 * c, w);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sh->qd_full));
+        }
         for (int n = 0; n < n_items && ok; ++n) {
             const int j = jlo + n;
             if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;

@@ -137,6 +137,8 @@ struct BwdParams {
     CUtensorMap tm_k;   // K and V with H_kv heads
     CUtensorMap tm_v;
     CUtensorMap tm_do;
+    const void* q;      // Q and dO as plain pointers too (Q's shape and layout): the dQ
+    const void* d_o;    // kernel reads its rows of them straight into TMEM
     void* dq;           // Q's shape and layout, input element type
     void* dk;           // K's shape and layout
     void* dv;
