@@ -1,0 +1,122 @@
+"""The decode split planner (CPU): the real C++ `decode_plan` from
+`csrc/fa_internal.h`, compiled here with the host compiler, checked against its
+contract.
+
+- Every plan covers the keys exactly once in chunks of 4-key groups.
+- With the kernel's residency given (CTAs per SM), the automatic plan takes at
+  most two waves of CTAs and no admissible split count fills its last wave
+  better; ties go to fewer splits; never more than ceil(Nk / 256) splits.
+- Without a residency (0) it keeps the older target of about eight CTAs per
+  SM, the rule the allocation-free decode entry point uses.
+"""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "attention_forward_16_gb300", "csrc")
+CUDA_INC = "/usr/local/cuda/include"
+
+DRIVER = r"""
+#include <cstdio>
+#include <cstdlib>
+#include "fa_internal.h"
+int main(int argc, char** argv) {
+    // each line of stdin: BH Nk sms n_req ctas_per_sm
+    long long BH; int Nk, sms, req, cps;
+    while (std::scanf("%lld %d %d %d %d", &BH, &Nk, &sms, &req, &cps) == 5) {
+        int ns = 0, chunk = 0;
+        fa::decode_plan(BH, Nk, sms, req, &ns, &chunk, cps);
+        std::printf("%d %d\n", ns, chunk);
+    }
+    return 0;
+}
+"""
+
+CASES = [
+    # (BH, Nk, sms, n_req, ctas_per_sm)
+    (64, 32768, 152, 0, 3),      # grouped-head decode, lane-group kernel
+    (256, 32768, 152, 0, 12),    # one query row per head, split kernel
+    (128, 4096, 152, 0, 3),      # four new tokens per head
+    (64, 32768, 152, 0, 0),      # the older rule
+    (1, 1, 152, 0, 3),
+    (1, 300, 152, 0, 3),
+    (4, 7, 152, 0, 3),
+    (2, 3000, 148, 0, 5),
+    (8, 65536, 152, 0, 1),
+    (5000, 4096, 152, 0, 3),     # more (b, h) than a wave: no split
+    (1, 5000, 152, 4, 3),        # explicit request wins
+    (2, 3000, 148, 100, 3),
+    (1, 65536, 152, 300, 0),
+]
+
+
+@pytest.fixture(scope="module")
+def plan_exe(tmp_path_factory):
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None or not os.path.isdir(CUDA_INC):
+        pytest.skip("host C++ compiler or CUDA headers not available")
+    d = tmp_path_factory.mktemp("plan")
+    src = d / "plan.cpp"
+    src.write_text(DRIVER)
+    exe = d / "plan"
+    subprocess.run([cxx, "-std=c++17", "-O1", "-I", CSRC, "-I", CUDA_INC, str(src), "-o", str(exe)], check=True,
+                   capture_output=True)
+    return str(exe)
+
+
+def _plans(exe, cases):
+    inp = "".join(" ".join(str(x) for x in c) + "\n" for c in cases)
+    out = subprocess.run([exe], input=inp, capture_output=True, text=True, check=True).stdout.split()
+    return [(int(out[2 * i]), int(out[2 * i + 1])) for i in range(len(cases))]
+
+
+def _eff(BH, t, slots):
+    waves = -(-BH * t // slots)
+    return BH * t / (waves * slots)
+
+
+def test_every_plan_covers_the_keys_once(plan_exe):
+    for (BH, Nk, sms, req, cps), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
+        assert ns >= 1 and chunk % 4 == 0
+        assert (ns - 1) * chunk < Nk <= ns * chunk, (BH, Nk, ns, chunk)
+
+
+def test_residency_plan_fills_its_last_wave_best(plan_exe):
+    for (BH, Nk, sms, req, cps), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
+        if req > 0 or cps == 0:
+            continue
+        slots = cps * sms
+        cap = -(-Nk // 256)
+        admissible = [t for t in range(1, cap + 1) if BH * t <= 2 * slots] or [1]
+        best = max(_eff(BH, t, slots) for t in admissible)
+        first_best = min(t for t in admissible if _eff(BH, t, slots) >= best - 1e-9)
+        # the planner's count, before chunk rounding, is the first best one
+        c = -(-Nk // first_best)
+        c = -(-c // 4) * 4
+        assert (ns, chunk) == (-(-Nk // c), c), (BH, Nk, cps, ns, first_best)
+        assert BH * ns <= 2 * slots or ns == 1
+        assert ns <= max(1, cap)
+
+
+def test_bench_shapes_get_one_wave(plan_exe):
+    cases = [(64, 32768, 152, 0, 3), (256, 32768, 152, 0, 12), (128, 4096, 152, 0, 3)]
+    assert [p[0] for p in _plans(plan_exe, cases)] == [7, 7, 7]
+
+
+def test_zero_residency_keeps_the_older_rule(plan_exe):
+    for BH, Nk, sms in [(64, 32768, 152), (8, 32768, 152), (256, 4096, 152), (2, 3000, 148)]:
+        (ns, chunk), = _plans(plan_exe, [(BH, Nk, sms, 0, 0)])
+        s = -(-8 * sms // BH)
+        s = max(1, min(s, -(-Nk // 256), Nk, 1024))
+        c = -(-Nk // s)
+        c = -(-c // 4) * 4
+        assert (ns, chunk) == (-(-Nk // c), c)
+
+
+def test_explicit_request_is_kept(plan_exe):
+    (ns, chunk), = _plans(plan_exe, [(1, 5000, 152, 4, 3)])
+    assert ns == 4 and chunk == 1252
