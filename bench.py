@@ -725,12 +725,69 @@ def run_reference_bwd(args, w, world, rank):
     return 0
 
 
+def run_reference_decode(args, w, world, rank):
+    """The float64 oracle on the host cores for a decode workload: each step is
+    the plain definition for one (b, K/V head) group of queries against its
+    whole cache (gathered through the block table when the cache is paged),
+    reported as GB/s of that group's compulsory bytes."""
+    if rank != 0:
+        return 0
+    from attention_forward_16_gb300.inputs import make_decode
+    from oracle import attention_grouped
+    q, k, v = make_decode(w)
+    Hkv = w.Hkv or w.H
+    G = w.H // Hkv
+    e = 4 if w.dtype == "f32" else 2
+    qd, kd, vd = (t.float().numpy() for t in (q, k, v))
+    sample = "one (b, K/V head) group of queries x its whole cache per step, float64 numpy"
+    if w.page_size:
+        from attention_forward_16_gb300.inputs import make_paged
+        from oracle.paged import gather_pages
+        kp, vp, tp = make_paged(w, k, v)
+        kc, vc, table = kp.float().numpy(), vp.float().numpy(), tp.numpy()
+        sample += ", gathered page by page through the block table"
+
+    def step(i):
+        b, hk = i % w.B, (i // w.B) % Hkv
+        if w.page_size:
+            ks = gather_pages(kc, table[b], w.Nk, w.page_size)[:, hk][None, None]   # [1, 1, Nk, D]
+            vs = gather_pages(vc, table[b], w.Nk, w.page_size)[:, hk][None, None]
+        else:
+            ks, vs = kd[b:b + 1, hk:hk + 1], vd[b:b + 1, hk:hk + 1]
+        attention_grouped(qd[b:b + 1, hk * G:(hk + 1) * G], ks, vs, w.scale, w.mask, w.win_l, w.win_r,
+                          q_offset=w.Nk - w.Nq)
+        return 2 * w.Nk * w.D * e + 2 * G * w.Nq * w.D * e + G * w.Nq * 4
+
+    for i in range(args.warmup):
+        step(i)
+    nbytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        nbytes += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": "attention decode HBM GB/s (split-K, K/V cache read once)", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": Hkv, "Nq": w.Nq, "Nk": w.Nk, "D": w.D,
+                   "page_size": w.page_size or None, "mask": w.mask, "step": "one (b, K/V head) group"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from attention_forward_16_gb300.inputs import DECODE_WORKLOADS, WORKLOADS
     if args.workload in DECODE_WORKLOADS:
         world, rank, local, pg = dist_setup(args)
         try:
+            if args.impl == "reference":
+                return run_reference_decode(args, DECODE_WORKLOADS[args.workload], world, rank)
             return run_decode(args, DECODE_WORKLOADS[args.workload], world, rank, local, pg)
         finally:
             if pg is not None:
