@@ -140,9 +140,12 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
  * FlashAttention API (workspace size query, then execute):
  *
  * fa_decode_plan -- for the current device, the number of splits a decode of
- *   this shape uses (n_splits <= 0: chosen to give about eight CTAs per SM with
- *   at least 256 keys each; > 0: that many, capped at Nk) and the workspace it
- *   needs in bytes (0 when one split suffices).  Returns FA_OK or FA_ERR_ARG.
+ *   this shape uses (n_splits <= 0: chosen from how many CTAs of the decode
+ *   kernel this shape takes fit on an SM, as the count of at most two waves
+ *   whose last wave is fullest, never more than ceil(Nk / 256); > 0: that
+ *   many, capped at Nk) and the workspace it needs in bytes (0 when one split
+ *   suffices).  The choice does not depend on the element type, and is fixed
+ *   for a device and shape.  Returns FA_OK or FA_ERR_ARG.
  *
  * fa_decode -- q [B, H, Nq, D], k and v [B, H, Nk, D], o [B, H, Nq, D] (element
  *   type dtype: FA_F16, FA_BF16 or FA_F32; D in {64, 128}), lse [B, H, Nq] fp32
@@ -225,9 +228,11 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
  * which every GPU that loads the library holds until the process exits.
  *
  * Returns FA_ERR_SCRATCH when the partials of this shape and split count would
- * not fit (fa_decode_plan's workspace size above the array's size; a smaller
- * n_splits or a call to fa_decode with a workspace is the way out), otherwise
- * the codes of fa_decode.  It allocates nothing.
+ * not fit (for an explicit n_splits, fa_decode_plan's workspace size above the
+ * array's size; a smaller n_splits or a call to fa_decode with a workspace is
+ * the way out), otherwise the codes of fa_decode.  It allocates nothing.  With
+ * n_splits <= 0 it picks its own split count, about eight CTAs per SM with at
+ * most ceil(Nk / 256) splits, which can differ from fa_decode_plan's choice.
  *
  * The first call on a device looks up the array's device address (once, with
  * that device current); make that first call before any stream capture.
