@@ -289,7 +289,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
         const uint32_t tDV = tmem + C::kColA, tDK = tmem + C::kColB;
         auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageKV; };
-        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1); };
+        auto ring_full = [&](int n) {
+            return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1);
+        };
         bool ok = W.wait_warp(smem_u32(&sh->fixed_full), 0) && ring_full(0);
         if (ok) {
             tc_fence_after();
@@ -483,7 +485,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColA;
         const uint32_t tQ = tmem + C::kColQ, tDO = tmem + C::kColDO;
         auto stage = [&](int n) { return sRing + (n % C::kStagesQ) * C::kStageQ; };
-        auto ring_full = [&](int n) { return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStagesQ]), (n / C::kStagesQ) & 1); };
+        auto ring_full = [&](int n) {
+            return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStagesQ]), (n / C::kStagesQ) & 1);
+        };
         // S = Q K^T and dP = dO V^T with the stationary A operand read from TMEM
         // (TS products): only K and V come from shared memory.
         auto rows_t = [&](uint32_t dst, uint32_t ta, uint32_t b) {
@@ -544,7 +548,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             const size_t qrow = (size_t)row_index(p.layout, b, h, live_q ? qi : 0, p.H, p.g.N);
             constexpr int kWords = D / 4;  // 32-bit words in half a row
             const uint16_t* srcs[2] = {static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o)};
-            const uint32_t dsts[2] = {tmem + lane_base + C::kColQ + hf * kWords, tmem + lane_base + C::kColDO + hf * kWords};
+            const uint32_t dsts[2] = {tmem + lane_base + C::kColQ + hf * kWords,
+                                      tmem + lane_base + C::kColDO + hf * kWords};
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 const uint4* src = reinterpret_cast<const uint4*>(srcs[x] + qrow * D + hf * (D / 2));
