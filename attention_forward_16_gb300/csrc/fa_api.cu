@@ -154,6 +154,10 @@ int validate(const void* q, const void* k, const void* v, const void* o, const f
 
 }  // namespace
 
+namespace fa {
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace fa
+
 extern "C" {
 
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
@@ -267,7 +271,7 @@ int fa_device_status(void* stream) {
 }
 
 unsigned long long fa_set_wait_limit_ns(unsigned long long ns) {
-    if (ns == 0) ns = 1;
+    if (ns < FA_MIN_WAIT_LIMIT_NS) ns = FA_MIN_WAIT_LIMIT_NS;
     return g_wait_limit_ns.exchange(ns);
 }
 

@@ -682,13 +682,17 @@ extern "C" int fa_decode_noalloc(const void* q, const void* k, const void* v, vo
     // Set-up, once per device, with that device current: the host-side name of
     // the array is not a device address, so ask the runtime for the real one.
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return FA_ERR_CUDA;
+    const cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return record_cuda_error(de);
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return record_cuda_error(cudaErrorInvalidDevice);
     NoAllocDevice& nd = g_noalloc_dev[dev];
     std::call_once(nd.once, [&] {
         nd.err = cudaGetSymbolAddress(&nd.scratch, g_decode_scratch);
         if (nd.err == cudaSuccess) nd.err = cudaDeviceGetAttribute(&nd.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (nd.err == cudaSuccess && !nd.scratch) nd.err = cudaErrorInvalidSymbol;
     });
-    if (nd.err != cudaSuccess || !nd.scratch) return FA_ERR_CUDA;
+    // A failed set-up is cached; every later call reports its error again.
+    if (nd.err != cudaSuccess) return record_cuda_error(nd.err);
 
     DecodeParams p;
     p.BH = (long long)B * H;
@@ -716,7 +720,7 @@ extern "C" int fa_decode_noalloc(const void* q, const void* k, const void* v, vo
     p.win_l = wl;
     p.win_r = wr;
     const cudaError_t e = launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return e == cudaSuccess ? FA_OK : record_cuda_error(e);
 }
 
 extern "C" unsigned long long fa_decode_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }

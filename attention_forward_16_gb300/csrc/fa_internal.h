@@ -174,6 +174,10 @@ struct RopeParams {
     int layout;
 };
 
+// Records `e` as this host thread's last CUDA error (the text
+// fa_last_cuda_error returns) and returns FA_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // Launchers (return the CUDA error of the launch, if any).
 cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s);
 // Resident CTAs per SM of the decode kernel that `rows` query rows per (b, K/V

@@ -139,14 +139,14 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
             }
         }
     }
-    if (!ok) {
-        // Let every issued copy land before shared memory is released.
-        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_it; ++s) {
-            const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::kStages);
-            W.drain(smem_u32(&sh->kv_full[s]), (last / C::kStages) & 1);
-        }
-        if (q_it > 0) W.drain(q_full, (q_it - 1) & 1);
+    // Let every issued copy land before shared memory is released.  This runs
+    // on the normal path too: if another role aborted, copies this thread
+    // issued may have no consumer left to wait for them.
+    for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_it; ++s) {
+        const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::kStages);
+        W.drain(smem_u32(&sh->kv_full[s]), (last / C::kStages) & 1);
     }
+    if (q_it > 0) W.drain(q_full, (q_it - 1) & 1);
 }
 
 // -------------------------------------------------------------- MMA issuers

@@ -60,12 +60,18 @@ struct Waiter {
         bool ok = wait(bar, parity);
         return __all_sync(0xffffffffu, ok);
     }
-    // Bounded wait that ignores the abort flag: lets in-flight async work land
-    // before the CTA releases its resources.
+    // Wait that ignores the abort flag: lets in-flight async work (TMA copies,
+    // tcgen05.mma) land before the CTA frees TMEM and its shared memory.  Its
+    // bound is kDrainLimitNs whatever the caller set as the ordinary wait
+    // limit: work already issued finishes in microseconds, so only a broken
+    // device reaches it, and a short ordinary limit can no longer cut a drain
+    // short while copies or MMAs are still writing.
+    static constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s
     __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) const {
         const uint64_t t0 = globaltimer_ns();
+        const unsigned long long bound = limit > kDrainLimitNs ? limit : kDrainLimitNs;
         while (!mbar_try_wait(bar, parity)) {
-            if (globaltimer_ns() - t0 > limit) {
+            if (globaltimer_ns() - t0 > bound) {
                 atomicExch(status, DEV_TIMEOUT);
                 return;
             }

@@ -356,8 +356,21 @@ int fa_rope_tables(float* cos_tab, float* sin_tab, int n_pos, int D, double base
  */
 int fa_device_status(void* stream);
 
-/* Wait limit, in nanoseconds, for every bounded wait inside the kernels of
- * this device (default 2e9).  Returns the previous value. */
+/* Smallest wait limit fa_set_wait_limit_ns accepts, in nanoseconds. */
+#define FA_MIN_WAIT_LIMIT_NS 1000ull
+
+/* Wait limit, in nanoseconds, for every bounded wait inside the kernels
+ * (default 2e9), taken by launches enqueued after the call.  Values below
+ * FA_MIN_WAIT_LIMIT_NS are raised to it.  Returns the previous value.
+ *
+ * A wait that runs past the limit makes the kernel stop early: it records
+ * FA_ERR_TIMEOUT for fa_device_status, and before it frees its tensor memory
+ * and shared memory it waits for the copies and tensor-core products it has
+ * already issued.  That final wait has its own fixed bound of one second (or
+ * the limit set here, if longer), so a short limit cannot end it while that
+ * work is still writing.  A limit below the time a launch's ordinary waits
+ * take (microseconds) therefore aborts the launch, with undefined outputs,
+ * but leaves the context usable. */
 unsigned long long fa_set_wait_limit_ns(unsigned long long ns);
 
 /*

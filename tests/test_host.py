@@ -268,3 +268,21 @@ def test_paged_decode_validation(lib, kw, code):
                              a["Nq"], a["max_seq"], a["ps"], a["max_pages"], a["num_pages"], a["D"], 0.1, 0, -1, -1,
                              a["dt"], 0, 0, None, 0, None)
     assert rc == code
+
+
+def test_wait_limit_setter_floor_and_round_trip(lib):
+    """The setter raises values below FA_MIN_WAIT_LIMIT_NS (1 us) to it and
+    returns the previous limit; it only stores a host value, so this needs
+    no GPU.  The kernels' final drain keeps its own 1 s bound whatever is set."""
+    floor = 1000
+    text = open(HEADER).read()
+    assert re.search(r"#define\s+FA_MIN_WAIT_LIMIT_NS\s+1000ull", text)
+    before = lib.fa_set_wait_limit_ns(0)
+    try:
+        assert lib.fa_set_wait_limit_ns(1) == floor          # 0 was raised to the floor
+        assert lib.fa_set_wait_limit_ns(floor - 1) == floor  # so was 1
+        assert lib.fa_set_wait_limit_ns(5_000_000) == floor
+        assert lib.fa_set_wait_limit_ns(7) == 5_000_000      # values at or above the floor are kept
+    finally:
+        lib.fa_set_wait_limit_ns(before)
+    assert lib.fa_set_wait_limit_ns(before) == before

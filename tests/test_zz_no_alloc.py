@@ -38,27 +38,38 @@ def _inputs(seed, B=2, H=4, Nq=2, Nk=3000, D=128, dtype="bf16"):
     return q.cuda(), k.cuda(), v.cuda()
 
 
-def _with_workspace(q, k, v, mk, stream):
+def _split_count(q, k):
+    """The split count fa_decode would choose for this shape.  Both entry
+    points are then given it explicitly: with the same splits they do the
+    same arithmetic in the same order, so the comparison is exact whatever
+    rule either one would use to choose its own count."""
+    B, H, Nq, D = q.shape
+    ns, wb = fb.fa_decode_plan(B, H, Nq, k.shape[2], D, 0)
+    assert ns > 1 and wb > 0, "the shape must need partials for the comparison to mean anything"
+    return ns
+
+
+def _with_workspace(q, k, v, mk, ns, stream):
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
-    ns, wb = fb.fa_decode_plan(B, H, Nq, Nk, D, 0)
-    assert ns > 1 and wb > 0, "the shape must need partials for the comparison to mean anything"
+    ns_out, wb = fb.fa_decode_plan(B, H, Nq, Nk, D, ns)
+    assert ns_out == ns
     ws = torch.empty(wb, dtype=torch.uint8, device="cuda")
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
     rc = fb.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, D,
-                      0.09, mk, -1, -1, fb.FA_BF16, 0, ws.data_ptr(), wb, stream)
+                      0.09, mk, -1, -1, fb.FA_BF16, ns, ws.data_ptr(), wb, stream)
     assert rc == fb.FA_OK
     return o, lse
 
 
-def _no_alloc(q, k, v, mk, stream):
+def _no_alloc(q, k, v, mk, ns, stream):
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
     rc = fb.fa_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
-                              D, 0.09, mk, -1, -1, fb.FA_BF16, 0, stream)
+                              D, 0.09, mk, -1, -1, fb.FA_BF16, ns, stream)
     assert rc == fb.FA_OK, fb.load().fa_strerror(rc)
     return o, lse
 
@@ -69,7 +80,8 @@ def test_no_alloc_matches_workspace_entry_point_twice_in_a_row():
     second = _inputs(seed=400)
     results = []
     for (q, k, v), mk in ((first, fb.FA_MASK_CAUSAL), (second, fb.FA_MASK_NONE)):
-        results.append((_no_alloc(q, k, v, mk, stream), _with_workspace(q, k, v, mk, stream)))
+        ns = _split_count(q, k)
+        results.append((_no_alloc(q, k, v, mk, ns, stream), _with_workspace(q, k, v, mk, ns, stream)))
     torch.cuda.synchronize()
     assert fb.fa_device_status(stream) == fb.FA_OK
     for (o_na, l_na), (o_ws, l_ws) in results:
