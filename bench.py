@@ -55,7 +55,15 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--also", default="auto",
+                    help="comma-separated forward workloads timed after the main one and reported under "
+                         "'also' ('auto': the causal and window benchmark shapes when the main workload is "
+                         "the default; 'none': skip)")
+    ap.add_argument("--also-steps", type=int, default=300)
     return ap.parse_args(argv)
+
+
+ALSO_DEFAULT = ("f16_causal_4k", "bf16_causal_4k", "bf16_window_16k")
 
 
 # ------------------------------------------------------------- helpers
@@ -279,6 +287,57 @@ def run_reference(args, w, world, rank):
 
 # ------------------------------------------------------------- native arm
 
+def time_forward_workload(w, args, device, pg, rank, local, peak):
+    """Time the fused forward alone on workload ``w`` (inputs resident in HBM,
+    larger than L2): ``args.also_steps`` launches after ``args.warmup``, each
+    bracketed by CUDA events on the launching stream, with the SM clocks
+    sampled meanwhile.  Returns a dict for the bench line's ``also`` key."""
+    import torch
+    import attention_forward_16_gb300 as fa
+    from attention_forward_16_gb300.flops import attention_flops
+    from attention_forward_16_gb300.inputs import make_workload
+
+    q, k, v = (t.to(device) for t in make_workload(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+    window = (w.win_l, w.win_r) if w.mask == fa.FA_MASK_WINDOW else None
+    causal = w.mask == fa.FA_MASK_CAUSAL
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.attention_fwd(q, k, v, scale=w.scale, causal=causal, window=window, out=o, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError(f"kernel reported a timeout during warm-up of {w.name}")
+    clocks = ClockSampler(local).start() if rank == 0 else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.also_steps)]
+    barrier(pg, device)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg, device)
+    clk = clocks.stop() if clocks else None
+    if fa.fa_device_status(stream.cuda_stream) != 0:
+        raise RuntimeError(f"kernel reported a timeout while timing {w.name}")
+    ms = reduce_max(pg, sum(a.elapsed_time(b) for a, b in ev) / len(ev), device)
+    flops = attention_flops(w.B, w.H, w.N, w.D, w.mask, w.win_l, w.win_r)
+    tf = flops / (ms / 1e3) / 1e12
+    del q, k, v, o, lse
+    return {"B": w.B, "H": w.H, "N": w.N, "D": w.D, "dtype": w.dtype, "mask": w.mask,
+            "window": [w.win_l, w.win_r], "input_scale": w.input_scale, "steps": args.also_steps,
+            "avg_launch_ms": ms, "algorithmic_flops_per_launch": flops, "TFLOP/s": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "kernel": "fa_fwd_tc_kernel<%d,%s>" % (w.D, w.dtype)},
+            "clocks": clk}
+
+
 def run_native(args, w, world, rank, local, pg):
     import torch
     import attention_forward_16_gb300 as fa
@@ -413,10 +472,23 @@ def run_native(args, w, world, rank, local, pg):
     if fa.fa_device_status(stream.cuda_stream) != 0:
         raise RuntimeError("kernel reported a timeout during the end-to-end steps")
 
-    if rank != 0:
-        return 0
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK_TFLOPS))
+    also = {}
+    if args.also == "auto":
+        names = ALSO_DEFAULT if args.workload == "f16_full_4k" and args.batch is None else ()
+    elif args.also == "none":
+        names = ()
+    else:
+        names = tuple(n for n in args.also.split(",") if n)
+    if names:
+        from attention_forward_16_gb300.inputs import WORKLOADS
+        for n in names:
+            also[n] = time_forward_workload(WORKLOADS[n], args, device, pg, rank, local, peak)
+            torch.cuda.empty_cache()
+
+    if rank != 0:
+        return 0
     achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
     traffic = recorded_traffic(w.name)
     line = {
@@ -442,6 +514,7 @@ def run_native(args, w, world, rank, local, pg):
                        "fused forward, D2H of O and LSE every step; "
                        "steps alternate over two streams so copies overlap the previous step's kernel"},
         "gpu_launches": args.steps * (2 if rope else 1),
+        "gpu_launches_also": sum(a["steps"] for a in also.values()),
     }
     if rope:
         hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -453,6 +526,8 @@ def run_native(args, w, world, rank, local, pg):
             "roofline": {"bound": "hbm", "achieved": rb / (rope_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                          "frac": rb / (rope_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": rb,
                          "peak_source": peak_src}}
+    if also:
+        line["also"] = also
     if world == 1 and not args.no_cpu_baseline:
         tf, desc, cores = cpu_oracle_sample(w, q, k, v, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
