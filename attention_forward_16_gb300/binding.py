@@ -55,6 +55,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]),
     "fa_rope": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "fa_rope_tables": (_I, [_P, _P, _I, _I, ctypes.c_double, _P]),
+    "fa_fwd_rope": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _I, _I, _I,
+                         _P]),
     "fa_device_status": (_I, [_P]),
     "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
@@ -195,6 +197,12 @@ def fa_rope(q, k, q_out, k_out, cos_tab, sin_tab, B, H, H_kv, Nq, Nk, D, q_pos0,
                           style, dtype, layout, stream)
 
 
+def fa_fwd_rope(q, k, v, o, lse, cos_tab, sin_tab, n_pos, q_pos0, style, B, H, H_kv, N, D, scale, mask_kind, win_l,
+                win_r, dtype, o_dtype, layout, stream):
+    return load().fa_fwd_rope(q, k, v, o, lse, cos_tab, sin_tab, n_pos, q_pos0, style, B, H, H_kv, N, D, scale,
+                              mask_kind, win_l, win_r, dtype, o_dtype, layout, stream)
+
+
 def fa_rope_tables(cos_tab, sin_tab, n_pos, D, base, stream):
     return load().fa_rope_tables(cos_tab, sin_tab, n_pos, D, base, stream)
 
@@ -238,7 +246,7 @@ def mask_args(causal=False, window=None):
 
 
 def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, out=None, lse=None,
-                  stream=None, layout="bhnd"):
+                  stream=None, layout="bhnd", rope=None, rope_style="half", rope_pos0=0):
     """O, LSE = softmax(scale * Q K^T + mask) V for CUDA tensors.
 
     ``layout="bhnd"``: q [B, H, N, D], k and v [B, H_kv, N, D];
@@ -248,6 +256,10 @@ def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, 
     (None or -1 for an unbounded side); ``scale`` defaults to 1/sqrt(D);
     ``o_dtype=torch.float32`` returns O in fp32 for 16-bit inputs.  Runs on
     the current CUDA stream unless ``stream`` (a torch.cuda.Stream) is given.
+
+    ``rope=(cos, sin)`` (fp32 [n_pos, D/2] tables, ``rope_tables``) rotates Q
+    inside the kernel (``fa_fwd_rope``): query row i at position
+    ``rope_pos0 + i``, pairing ``rope_style``.  K must already be rotated.
     """
     if layout not in _LAYOUT_CODE:
         raise ValueError(f"layout must be one of {sorted(_LAYOUT_CODE)}")
@@ -279,6 +291,20 @@ def attention_fwd(q, k, v, scale=None, causal=False, window=None, o_dtype=None, 
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     s = (stream or torch.cuda.current_stream(q.device)).cuda_stream
+    if rope is not None:
+        cos, sin = rope
+        if rope_style not in _ROPE_STYLE:
+            raise ValueError(f"rope_style must be one of {sorted(_ROPE_STYLE)}")
+        if (cos.dtype != torch.float32 or sin.shape != cos.shape or cos.dim() != 2 or cos.shape[1] != D // 2
+                or not (cos.is_cuda and sin.is_cuda and cos.is_contiguous() and sin.is_contiguous())):
+            raise ValueError("rope tables must be contiguous fp32 CUDA tensors [n_pos, D/2] of one shape")
+        with torch.cuda.device(q.device):
+            rc = fa_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                             cos.data_ptr(), sin.data_ptr(), cos.shape[0], int(rope_pos0), _ROPE_STYLE[rope_style],
+                             B, H, Hkv, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od],
+                             _LAYOUT_CODE[layout], s)
+        _check(rc, "fa_fwd_rope")
+        return out, lse
     with torch.cuda.device(q.device):
         rc = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                         B, H, Hkv, N, D, float(scale), mk, wl, wr, _DTYPE_CODE[q.dtype], _DTYPE_CODE[od],
@@ -438,10 +464,15 @@ def apply_rope(q=None, k=None, cos=None, sin=None, style="half", q_pos0=0, k_pos
     return q_out, k_out
 
 
-def attention_fwd_rope(q, k, v, cos, sin, style="half", pos0=0, layout="bhnd", **kw):
-    """attention_fwd on rotary-embedded q and k: ``fa_rope`` writes the
-    rotated copies (rows at positions pos0, pos0 + 1, ...), then the fused
-    forward runs on them.  Returns (O, LSE)."""
+def attention_fwd_rope(q, k, v, cos, sin, style="half", pos0=0, layout="bhnd", fused=True, **kw):
+    """attention_fwd on rotary-embedded q and k (rows at positions pos0,
+    pos0 + 1, ...).  For fp16 / bf16 with ``fused=True`` only K goes through
+    the ``fa_rope`` pass and Q is rotated inside the attention kernel
+    (``fa_fwd_rope``); otherwise ``fa_rope`` writes rotated copies of both
+    and the plain forward runs on them.  Returns (O, LSE)."""
+    if fused and q.dtype in (torch.float16, torch.bfloat16):
+        _, kr = apply_rope(None, k, cos, sin, style=style, k_pos0=pos0, layout=layout, stream=kw.get("stream"))
+        return attention_fwd(q, kr, v, layout=layout, rope=(cos, sin), rope_style=style, rope_pos0=pos0, **kw)
     qr, kr = apply_rope(q, k, cos, sin, style=style, q_pos0=pos0, k_pos0=pos0, layout=layout,
                         stream=kw.get("stream"))
     return attention_fwd(qr, kr, v, layout=layout, **kw)

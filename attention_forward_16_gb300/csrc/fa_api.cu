@@ -158,16 +158,25 @@ namespace fa {
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 }  // namespace fa
 
-extern "C" {
+namespace {
 
-int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+// Rotary embedding of Q inside the forward (null tables: none).
+struct RopeQ {
+    const float* cos = nullptr;
+    const float* sin = nullptr;
+    int style = 0;
+    int pos0 = 0;
+};
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
                int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout,
-               void* stream) {
+               const RopeQ& rope, void* stream) {
     fa::Geom g;
     int rc = validate(q, k, v, o, lse, B, H, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, &g);
     if (rc != FA_OK) return rc;
     if (H_kv <= 0 || H_kv > H || H % H_kv != 0) return FA_ERR_ARG;
     if (layout != FA_LAYOUT_BHND && layout != FA_LAYOUT_BNHD) return FA_ERR_ARG;
+    if (rope.cos && dtype == FA_F32) return FA_ERR_UNSUPPORTED;
     DeviceInfo* dev;
     if ((rc = device_info(&dev)) != FA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -212,9 +221,43 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
     p.o_f32 = o_dtype == FA_F32 ? 1 : 0;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.status = dev->status;
+    if (rope.cos) {
+        p.rope = 1;
+        p.rope_cos = rope.cos;
+        p.rope_sin = rope.sin;
+        p.rope_style = rope.style;
+        p.rope_pos0 = rope.pos0;
+    }
     const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
     cudaError_t e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+               int D, float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout,
+               void* stream) {
+    return fwd_common(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, layout,
+                      RopeQ{}, stream);
+}
+
+int fa_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, const float* cos_tab,
+                const float* sin_tab, int n_pos, int q_pos0, int style, int B, int H, int H_kv, int N, int D,
+                float scale, int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout, void* stream) {
+    if (!cos_tab || !sin_tab || n_pos <= 0 || q_pos0 < 0) return FA_ERR_ARG;
+    if (N > 0 && (long long)q_pos0 + N > n_pos) return FA_ERR_ARG;
+    if (style != fa::ROPE_HALF && style != fa::ROPE_INTERLEAVED) return FA_ERR_ARG;
+    if (!aligned(cos_tab, 16) || !aligned(sin_tab, 16)) return FA_ERR_ALIGN;
+    RopeQ r;
+    r.cos = cos_tab;
+    r.sin = sin_tab;
+    r.style = style;
+    r.pos0 = q_pos0;
+    return fwd_common(q, k, v, o, lse, B, H, H_kv, N, D, scale, mask_kind, win_l, win_r, dtype, o_dtype, layout, r,
+                      stream);
 }
 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,

@@ -173,6 +173,18 @@ FA_HD Unit make_unit(const Geom& g, int BH, int order, int u) {
     return un;
 }
 
+// The unit a persistent CTA takes in round r: rounds hand out `ctas`
+// consecutive units, in CTA order on even rounds and in reverse order on odd
+// ones.  Units come longest first under masks whose work varies by query
+// tile, so plain round robin would give the low CTAs the longer unit of every
+// round; alternating the direction pairs a longer unit with a shorter one and
+// evens out the total per CTA.  Once r * ctas + (unit offset) passes the last
+// unit, no later round has one for this CTA either.
+FA_HD int sched_unit(int r, int cta, int ctas) {
+    const long long u = (long long)r * ctas + ((r & 1) ? ctas - 1 - cta : cta);
+    return u > 0x7fffffffLL ? 0x7fffffff : (int)u;  // past any unit count
+}
+
 FA_HD int unit_order_for(const Geom& g) {
     if (g.win_r >= 0) return ORDER_Q_DESC;   // causal-like: later rows see more keys
     if (g.win_l >= 0) return ORDER_Q_ASC;    // earlier rows see more keys

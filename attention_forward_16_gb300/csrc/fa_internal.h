@@ -38,6 +38,13 @@ struct TcParams {
     int o_f32;
     unsigned long long wait_limit_ns;
     int* status;        // device status word
+    // Rotary embedding of Q applied in the kernel (rope != 0): query row i
+    // sits at position rope_pos0 + i of the fp32 [n_pos, D/2] cos/sin tables.
+    const float* rope_cos;
+    const float* rope_sin;
+    int rope;
+    int rope_style;     // RopeStyle
+    int rope_pos0;
 };
 
 struct SimtParams {

@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.h"
+#include "rope_math.cuh"
 
 namespace fa {
 namespace {
@@ -130,18 +131,13 @@ __global__ void __launch_bounds__(256) fa_rope_kernel(const RopeParams p) {
             if (kStyle == ROPE_HALF) {
                 // pair m: (u[m], v[m]) with table column 8g + m
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    yu[m] = u[m] * c[m] - v[m] * s[m];
-                    yv[m] = v[m] * c[m] + u[m] * s[m];
-                }
+                for (int m = 0; m < 8; ++m) rope_rotate(u[m], v[m], c[m], s[m], yu[m], yv[m]);
             } else {
                 // pairs (u[2m], u[2m+1]) with column 8g + m, (v[2m], v[2m+1]) with 8g + 4 + m
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    yu[2 * m] = u[2 * m] * c[m] - u[2 * m + 1] * s[m];
-                    yu[2 * m + 1] = u[2 * m + 1] * c[m] + u[2 * m] * s[m];
-                    yv[2 * m] = v[2 * m] * c[4 + m] - v[2 * m + 1] * s[4 + m];
-                    yv[2 * m + 1] = v[2 * m + 1] * c[4 + m] + v[2 * m] * s[4 + m];
+                    rope_rotate(u[2 * m], u[2 * m + 1], c[m], s[m], yu[2 * m], yu[2 * m + 1]);
+                    rope_rotate(v[2 * m], v[2 * m + 1], c[4 + m], s[4 + m], yv[2 * m], yv[2 * m + 1]);
                 }
             }
             Vec8<T>::store(y + r + oa, yu);

@@ -14,9 +14,9 @@
 //   warps 0-3   Q tile 0: softmax (thread = one query row), then its epilogue
 //   warps 4-7   Q tile 1: same
 //   warp  8     TMEM allocator; issues Q tile 0's tcgen05.mma (one elected lane)
-//   warp  9     one thread issues every TMA load (Q tiles, K/V ring)
+//   warp  9     one thread issues the TMA loads of the K/V ring
 //   warp  10    issues Q tile 1's tcgen05.mma (one elected lane)
-//   warp  11    idle (completes the third warpgroup)
+//   warp  11    one thread issues the TMA loads of the two Q tiles
 //
 // The launch gives 168 registers a thread (12 warps, three per SM
 // sub-partition); setmaxnreg then moves 48 from the MMA/TMA warpgroup to the
@@ -38,6 +38,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 #include "tc_common.cuh"
 
 namespace fa {
@@ -57,6 +58,7 @@ static_assert(2 * kRegSoftmax + kRegOther <= 3 * kLaunchRegs, "register split ex
 constexpr int kWarpMma = 8;    // MMA issuer for Q tile 0; TMEM owner
 constexpr int kWarpTma = 9;
 constexpr int kWarpMma1 = 10;  // MMA issuer for Q tile 1
+constexpr int kWarpTmaQ = 11;  // Q tile loads
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -75,7 +77,8 @@ struct TcCfg {
 };
 
 struct __align__(16) SharedCtl {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];  // per Q tile
+    uint64_t q_ready[2];             // per Q tile: rotated in place (rotary embedding of Q)
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t drain[2];
@@ -96,34 +99,72 @@ static_assert(smem_bytes<128>() <= 227 * 1024, "shared memory budget (D=128)");
 static_assert(TcCfg<128>::kStages >= 4 && TcCfg<64>::kStages >= 4, "K/V ring too short for the issue order");
 static_assert(smem_bytes<64>() <= 227 * 1024, "shared memory budget (D=64)");
 
-// ------------------------------------------------------------- TMA producer
+// ------------------------------------------------------------ TMA producers
+// Tensor-map coordinates (d, row, head, batch) of a 128-row x 64-column box;
+// rows and heads trade places for [B, N, H, D].
+__device__ __forceinline__ void load_box(const TcParams& p, uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c,
+                                         int row, int head, int b) {
+    if (p.layout == LAYOUT_BHND)
+        tma_load_4d(dst, tm, bar, c * 64, row, head, b);
+    else
+        tma_load_4d(dst, tm, bar, c * 64, head, row, b);
+}
+
+// Q tiles: one thread, one buffer per tile.  Tile t of the next unit is loaded
+// as soon as tile t's last S of the current unit has completed, so a tile that
+// finishes its key range first (tile 0 under causal and window masks) can
+// start its next unit while the other tile finishes this one.  K/V loads have
+// their own thread and never wait behind a Q buffer.
 template <int D>
-__device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
-                                         uint32_t sKVa) {
+__device__ __forceinline__ void tma_q_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa) {
     using C = TcCfg<D>;
     tma_prefetch_desc(&p.tm_q);
+    uint32_t q_it[2] = {0, 0};
+    bool ok = true;
+    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
+        const Unit un = make_unit(p.g, p.BH, p.order, u);
+        const int b = un.bh / p.H, h = un.bh % p.H;
+        for (int t = 0; t < 2 && ok; ++t) {
+            const uint32_t q_full = smem_u32(&sh->q_full[t]);
+            if (q_it[t] > 0 && !(ok = W.wait(smem_u32(&sh->q_empty[t]), (q_it[t] - 1) & 1))) break;
+            mbar_arrive_expect_tx(q_full, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                load_box(p, sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c, un.q0 + t * kTileM, h, b);
+            ++q_it[t];
+        }
+        // Pull this CTA's next Q tiles into L2 now: their loads wait for this
+        // unit's last S products, and would otherwise start with a DRAM latency.
+        const int un_next = sched_unit(r + 1, blockIdx.x, gridDim.x);
+        if (ok && un_next < p.n_units) {
+            const Unit nx = make_unit(p.g, p.BH, p.order, un_next);
+            const int nb = nx.bh / p.H, nh = nx.bh % p.H;
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < C::kChunks; ++c) {
+                    if (p.layout == LAYOUT_BHND)
+                        tma_prefetch_l2_4d(&p.tm_q, c * 64, nx.q0 + t * kTileM, nh, nb);
+                    else
+                        tma_prefetch_l2_4d(&p.tm_q, c * 64, nh, nx.q0 + t * kTileM, nb);
+                }
+        }
+    }
+    // Let every issued copy land before shared memory is released (on the
+    // normal path too: after an abort elsewhere nobody may wait for them).
+    for (int t = 0; t < 2; ++t)
+        if (q_it[t] > 0) W.drain(smem_u32(&sh->q_full[t]), (q_it[t] - 1) & 1);
+}
+
+// K/V tiles: one thread filling the ring, K_j then V_j for every key tile in
+// the union of the unit's two ranges.
+template <int D>
+__device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sKVa) {
+    using C = TcCfg<D>;
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
-    const uint32_t q_full = smem_u32(&sh->q_full);
-    const uint32_t q_empty = smem_u32(&sh->q_empty);
-    uint32_t kv_it = 0, q_it = 0;
+    uint32_t kv_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         const int b = un.bh / p.H, h = un.bh % p.H, hk = h / p.G;
-        // Tensor-map coordinates (d, row, head, batch), rows and heads swapped for [B,N,H,D].
-        auto load = [&](uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c, int row, int head) {
-            if (p.layout == LAYOUT_BHND)
-                tma_load_4d(dst, tm, bar, c * 64, row, head, b);
-            else
-                tma_load_4d(dst, tm, bar, c * 64, head, row, b);
-        };
-        if (q_it > 0 && !(ok = W.wait(q_empty, (q_it - 1) & 1))) break;
-        mbar_arrive_expect_tx(q_full, 2 * C::kTileBytes);
-        for (int t = 0; t < 2; ++t)
-            for (int c = 0; c < C::kChunks; ++c)
-                load(sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c, un.q0 + t * kTileM, h);
-        ++q_it;
         for (int j = un.jlo; j < un.jhi && ok; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const int slot = kv_it % C::kStages;
@@ -134,28 +175,25 @@ __device__ __forceinline__ void tma_role(const TcParams& p, const Waiter& W, Sha
                 mbar_arrive_expect_tx(full, C::kTileBytes);
                 const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
                 for (int c = 0; c < C::kChunks; ++c)
-                    load(sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c, j * kTileN, hk);
+                    load_box(p, sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c, j * kTileN, hk, b);
                 ++kv_it;
             }
         }
     }
-    // Let every issued copy land before shared memory is released.  This runs
-    // on the normal path too: if another role aborted, copies this thread
-    // issued may have no consumer left to wait for them.
+    // Let every issued copy land before shared memory is released.
     for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_it; ++s) {
         const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::kStages);
         W.drain(smem_u32(&sh->kv_full[s]), (last / C::kStages) & 1);
     }
-    if (q_it > 0) W.drain(q_full, (q_it - 1) & 1);
 }
 
 // -------------------------------------------------------------- MMA issuers
 // One issuing warp per Q tile t: S_t(j) = Q_t K_j^T and O_t += P_t(j) V_j.
 // Each warp keeps its own tile's order (S_t(j+1) after P.V_t(j), since P
-// aliases S).  A K/V ring slot and the Q buffer are released once both warps
-// have arrived (count 2); a tile with no work on key tile j still waits for
-// that slot to be full before arriving, which keeps the phases of the ring
-// aligned.
+// aliases S).  A K/V ring slot is released once both warps have arrived
+// (count 2); a tile with no work on key tile j still waits for that slot to
+// be full before arriving, which keeps the phases of the ring aligned.  Each
+// Q tile's buffer is released by its own warp once its last S has completed.
 //
 // The whole warp runs this role on one path: every wait, counter and shared-
 // memory descriptor is warp-uniform, and one elected lane issues the
@@ -179,8 +217,10 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     const uint32_t p_full = smem_u32(&sh->p_full[t]);
     const uint32_t o_done = smem_u32(&sh->o_done[t]);
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
-    const uint32_t q_full = smem_u32(&sh->q_full);
-    const uint32_t q_empty = smem_u32(&sh->q_empty);
+    // With the rotary embedding of Q the tile is released to this warp by its
+    // softmax warpgroup once rotated; otherwise as soon as its copy lands.
+    const uint32_t q_full = smem_u32(p.rope ? &sh->q_ready[t] : &sh->q_full[t]);
+    const uint32_t q_empty = smem_u32(&sh->q_empty[t]);
     const bool leader = elect_one();
     uint32_t kv_it = 0, q_it = 0, p_cnt = 0, o_cnt = 0;
     bool ok = true;
@@ -261,7 +301,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         return true;
     };
 
-    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         if (!(ok = W.wait_warp(q_full, q_it & 1))) break;
         ++q_it;
@@ -323,10 +363,65 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     W.drain(drain, 0);
 }
 
+// ------------------------------------------- rotary embedding of a Q tile
+// One query row of a Q tile in shared memory, rotated in place by the table
+// entries of its position (the rotation of "Ascend C advanced practice:
+// high-performance FlashAttention-2-style tile-level fused attention",
+// section 9, applied to Q as it is loaded; K arrives already rotated).  The
+// tile holds D/64 column chunks of 128 rows x 128 bytes, 128-byte swizzled:
+// 16-byte unit U of row r sits at chunk U/8, slot (U%8) ^ (r%8).  Groups of
+// eight pairs: half-split pairs units g and D/16 + g element by element,
+// interleaved pairs neighbours inside units 2g and 2g + 1.
+template <int D, bool kBf16>
+__device__ __forceinline__ void rope_q_row(uint8_t* tile, int row, const float* cos_row, const float* sin_row,
+                                           int style) {
+    constexpr int kBox = TcCfg<D>::kBoxBytes;
+    uint8_t* rb = tile + row * 128;
+    const int sw = row & 7;
+#pragma unroll
+    for (int g = 0; g < D / 16; ++g) {
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(cos_row + 8 * g));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(cos_row + 8 * g + 4));
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(sin_row + 8 * g));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(sin_row + 8 * g + 4));
+        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const int ua = style == ROPE_HALF ? g : 2 * g;
+        const int ub = style == ROPE_HALF ? D / 16 + g : 2 * g + 1;
+        uint4* pa = reinterpret_cast<uint4*>(rb + (ua >> 3) * kBox + (((ua & 7) ^ sw) << 4));
+        uint4* pb = reinterpret_cast<uint4*>(rb + (ub >> 3) * kBox + (((ub & 7) ^ sw) << 4));
+        const uint4 wa = *pa, wb = *pb;
+        const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
+        const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
+        float u[8], v[8], yu[8], yv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            u[2 * i] = lo_half<kBf16>(xa[i]);
+            u[2 * i + 1] = hi_half<kBf16>(xa[i]);
+            v[2 * i] = lo_half<kBf16>(xb[i]);
+            v[2 * i + 1] = hi_half<kBf16>(xb[i]);
+        }
+        if (style == ROPE_HALF) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) rope_rotate(u[m], v[m], c[m], sn[m], yu[m], yv[m]);
+        } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                rope_rotate(u[2 * m], u[2 * m + 1], c[m], sn[m], yu[2 * m], yu[2 * m + 1]);
+                rope_rotate(v[2 * m], v[2 * m + 1], c[4 + m], sn[4 + m], yv[2 * m], yv[2 * m + 1]);
+            }
+        }
+        *pa = make_uint4(pack2<kBf16>(yu[0], yu[1]), pack2<kBf16>(yu[2], yu[3]), pack2<kBf16>(yu[4], yu[5]),
+                         pack2<kBf16>(yu[6], yu[7]));
+        *pb = make_uint4(pack2<kBf16>(yv[0], yv[1]), pack2<kBf16>(yv[2], yv[3]), pack2<kBf16>(yv[4], yv[5]),
+                         pack2<kBf16>(yv[6], yv[7]));
+    }
+}
+
 // ------------------------------------------------------ softmax + epilogue
 template <int D, bool kBf16, bool kPosScale>
 __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t tmem,
-                                             int warp, int lane) {
+                                             uint8_t* sQ, int warp, int lane) {
     using C = TcCfg<D>;
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -339,15 +434,29 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     const uint32_t o_done = smem_u32(&sh->o_done[t]);
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
     const float c2 = p.scale_log2;
-    uint32_t s_cnt = 0, u_cnt = 0;
+    uint32_t s_cnt = 0, u_cnt = 0, q_cnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         const int jlo_t = t ? un.lo[1] : un.lo[0];
         const int jhi_t = t ? un.hi[1] : un.hi[0];
-        if (jlo_t == jhi_t) continue;
         const int r0 = un.q0 + t * kTileM;
         const int qi = r0 + row;
+        if (p.rope) {
+            // Rotate this thread's row of the tile once it has landed, make the
+            // stores visible to the tensor core, and release the tile (every
+            // unit, so the issuer's phases stay aligned even for an empty tile).
+            if (!(ok = W.wait_warp(smem_u32(&sh->q_full[t]), q_cnt & 1))) break;
+            ++q_cnt;
+            if (jlo_t < jhi_t && qi < p.g.N) {
+                const long long pos = (long long)p.rope_pos0 + qi;
+                rope_q_row<D, kBf16>(sQ + t * C::kTileBytes, row, p.rope_cos + pos * (D / 2),
+                                     p.rope_sin + pos * (D / 2), p.rope_style);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&sh->q_ready[t]));
+        }
+        if (jlo_t == jhi_t) continue;
         const bool split = kBf16 && tile_split_p(p.g, r0);
         float m_ref = -INFINITY;
         float l = 0.f;
@@ -525,8 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&sh->q_full), 1);
-        mbar_init(smem_u32(&sh->q_empty), 2);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&sh->q_full[t]), 1);
+            mbar_init(smem_u32(&sh->q_empty[t]), 1);
+            mbar_init(smem_u32(&sh->q_ready[t]), 128);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&sh->kv_full[s]), 1);
             mbar_init(smem_u32(&sh->kv_empty[s]), 2);
@@ -562,11 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
         setmaxnreg_inc<kRegSoftmax>();
 
     if (warp < 8) {
-        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, warp, lane);
+        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, smem, warp, lane);
     } else if (warp == kWarpMma || warp == kWarpMma1) {
         mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
     } else if (warp == kWarpTma) {
-        if (lane == 0) tma_role<D>(p, W, sh, sQa, sKVa);
+        if (lane == 0) tma_kv_role<D>(p, W, sh, sKVa);
+    } else if (warp == kWarpTmaQ) {
+        if (lane == 0) tma_q_role<D>(p, W, sh, sQa);
     }
 
     tc_fence_before();

@@ -110,6 +110,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Prefetch one box of a 4-D tensor map into L2 (no shared-memory
+// destination, no completion to wait for; boxes past the tensor's edge are
+// clipped like loads).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global into shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

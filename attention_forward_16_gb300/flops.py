@@ -46,10 +46,11 @@ def algorithmic_bytes(B, H, N, D, dtype, o_dtype=None, with_lse=True):
     return B * H * N * D * (3 * e + eo) + (B * H * N * 4 if with_lse else 0)
 
 
-def rope_bytes(w):
-    """Compulsory bytes of the rotary embedding pass of workload ``w``: Q and
-    K read and their rotated copies written, plus the cos/sin table read
-    once."""
+def rope_bytes(w, tensors=1):
+    """Compulsory bytes of the rotary embedding pass of workload ``w`` over
+    ``tensors`` of Q and K (1: K alone, the pass the fused forward leaves;
+    2: both): each read and its rotated copy written, plus the cos/sin table
+    read once."""
     esize = {"f16": 2, "bf16": 2, "f32": 4}[w.dtype]
-    qk = 2 * w.B * w.H * w.N * w.D * esize
-    return 2 * qk + 2 * w.N * (w.D // 2) * 4
+    x = tensors * w.B * w.H * w.N * w.D * esize
+    return 2 * x + 2 * w.N * (w.D // 2) * 4

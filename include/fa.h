@@ -316,11 +316,13 @@ enum {
  * (of K: k_pos0 + n), and each of its D/2 pairs (x_a, x_b), pair i, becomes
  *     x_a' = x_a cos_tab[p][i] - x_b sin_tab[p][i]
  *     x_b' = x_b cos_tab[p][i] + x_a sin_tab[p][i]
- * in fp32, rounded once to the element type.  Here it is one streaming pass
- * over Q and K in device memory rather than a step inside the attention
- * kernel's tile loads: each K tile is loaded by every CTA of its head, so a
- * rotation there would be repeated N/256 times per head and would compete for
- * the shared-memory bandwidth the tensor-core products need.
+ * in fp32 (x_b sin and x_a sin rounded once, the rest fused), rounded once
+ * to the element type.  This entry point is one streaming pass over Q and/or
+ * K in device memory.  For the forward, fa_fwd_rope rotates Q inside the
+ * attention kernel as its tiles arrive (Q is loaded once per work unit, so
+ * nothing is repeated); K stays a pass of its own here, because each K tile
+ * is loaded by every CTA of its head and a rotation at the load would be
+ * repeated N/256 times per head.
  *
  * q, q_out: [B, H, Nq, D] (FA_LAYOUT_BHND) or [B, Nq, H, D] (FA_LAYOUT_BNHD).
  * k, k_out: [B, H_kv, Nk, D] or [B, Nk, H_kv, D].  dtype: FA_F16, FA_BF16 or
@@ -338,6 +340,32 @@ enum {
 int fa_rope(const void* q, const void* k, void* q_out, void* k_out, const float* cos_tab, const float* sin_tab,
             int B, int H, int H_kv, int Nq, int Nk, int D, int q_pos0, int k_pos0, int n_pos,
             int style, int dtype, int layout, void* stream);
+
+/*
+ * fa_fwd_rope -- fa_fwd_gqa with the rotary embedding of Q applied inside the
+ * kernel, as "Ascend C advanced practice: high-performance
+ * FlashAttention-2-style tile-level fused attention", section 9, describes:
+ * each 128-row Q tile is rotated in shared memory right after its copy lands
+ * and before its first Q K^T product.  Query row i sits at position
+ * q_pos0 + i and is rotated exactly as fa_rope rotates it (same formula, same
+ * rounding, so the result equals fa_rope on Q followed by fa_fwd_gqa bit for
+ * bit).  K must already be rotated (fa_rope with q = NULL, or a cache of
+ * rotated keys); V is not rotated.
+ *
+ * cos_tab, sin_tab: fp32 [n_pos, D/2] device tables (fa_rope_tables), 16-byte
+ * aligned; style FA_ROPE_HALF or FA_ROPE_INTERLEAVED.  The other arguments,
+ * layouts and outputs are those of fa_fwd_gqa; dtype FA_F16 or FA_BF16.
+ *
+ * Returns FA_OK, FA_ERR_ARG (missing table, n_pos <= 0, q_pos0 < 0,
+ * q_pos0 + N > n_pos, bad style, or any fa_fwd_gqa argument error),
+ * FA_ERR_UNSUPPORTED (FA_F32, or fa_fwd_gqa's limits), FA_ERR_ALIGN or
+ * FA_ERR_CUDA.
+ */
+int fa_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse,
+                const float* cos_tab, const float* sin_tab, int n_pos, int q_pos0, int style,
+                int B, int H, int H_kv, int N, int D, float scale,
+                int mask_kind, int win_l, int win_r, int dtype, int o_dtype, int layout,
+                void* stream);
 
 /*
  * fa_rope_tables -- fill cos_tab and sin_tab (fp32 [n_pos, D/2], caller-owned

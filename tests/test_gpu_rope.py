@@ -171,3 +171,60 @@ def test_full_size_rotation_sampled_rows():
             x = src[b, h, n:n + 1].double().numpy()[None, None]
             got = out[b, h, n:n + 1].float().cpu().double().numpy()[None, None]
             _check_rot(got, x, c64, s64, "half", n, "f16", -2, f"row ({b},{h},{n})")
+
+
+# ------------------------------------------- rotation of Q inside the forward
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("style", ["half", "interleaved"])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+@pytest.mark.parametrize("D,N", [(64, 300), (128, 129), (128, 640)])
+def test_fused_q_rotation_equals_separate_pass_bit_for_bit(dtype, style, layout, D, N):
+    """fa_fwd_rope rotates each Q tile in shared memory with the same
+    arithmetic as fa_rope (one shared helper, the same rounding), so the
+    fused forward must give exactly the bits of fa_rope on Q followed by the
+    plain forward: for every mask, grouped heads, a ragged tail and rows that
+    start at a nonzero position."""
+    B, H, Hkv, pos0 = 2, 4, 2, 37
+    q, _, _ = make_qkv(B, H, N, D, dtype, seed=40 + D + N, n_k=1)
+    _, k, v = make_qkv(B, Hkv, 1, D, dtype, seed=41 + D + N, n_k=N)
+    if layout == "bnhd":
+        q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in (q, k, v))
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    cos, sin = fa.rope_tables(pos0 + N + 5, D, 10000.0)
+    _, kr = fa.apply_rope(None, k, cos, sin, style=style, k_pos0=pos0, layout=layout)
+    qr, _ = fa.apply_rope(q, None, cos, sin, style=style, q_pos0=pos0, layout=layout)
+    for causal, window in ((False, None), (True, None), (False, (50, 3))):
+        o1, l1 = fa.attention_fwd(q, kr, v, causal=causal, window=window, layout=layout, rope=(cos, sin),
+                                  rope_style=style, rope_pos0=pos0)
+        o2, l2 = fa.attention_fwd(qr, kr, v, causal=causal, window=window, layout=layout)
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), (causal, window)
+    # Q itself is not modified: the rotation happens on the tile in shared memory
+    assert not torch.equal(q, qr)
+
+
+def test_fused_q_rotation_full_size_benchmark_shape():
+    """B=4, H=32, N=4096, D=128 fp16 (the benchmark shape with rotary
+    embedding): many units per CTA, every Q tile rotated in place once; equal
+    bit for bit to the two-pass path, and within the forward's bound of the
+    oracle on sampled rows."""
+    B, H, N, D = 4, 32, 4096, 128
+    q, k, v = make_qkv(B, H, N, D, "f16", seed=1003)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    cos, sin = fa.rope_tables(N, D, 10000.0)
+    qr, kr = fa.apply_rope(q, k, cos, sin)
+    o1, l1 = fa.attention_fwd(q, kr, v, rope=(cos, sin))
+    o2, l2 = fa.attention_fwd(qr, kr, v)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    from oracle import attention_three_pass
+    qd, kd, vd = (t.double().cpu().numpy() for t in (qr, kr, v))
+    o1, l1 = o1.float().cpu().numpy().astype(np.float64), l1.cpu().numpy().astype(np.float64)
+    for b, h, r0 in ((0, 0, 0), (3, 31, 4032), (1, 17, 2000)):
+        ro, rl = attention_three_pass(qd[b:b + 1, h:h + 1, r0:r0 + 64], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                                      1.0 / math.sqrt(D), MASK_NONE, q_offset=r0)
+        assert (np.abs(o1[b, h, r0:r0 + 64] - ro[0, 0]) - _half_ulp(ro[0, 0], "f16")).max() <= 2e-3
+        assert np.abs(l1[b, h, r0:r0 + 64] - rl[0, 0]).max() <= 1e-3

@@ -286,3 +286,19 @@ def test_wait_limit_setter_floor_and_round_trip(lib):
     finally:
         lib.fa_set_wait_limit_ns(before)
     assert lib.fa_set_wait_limit_ns(before) == before
+
+
+def test_fwd_rope_rejections_before_any_launch(lib):
+    """fa_fwd_rope validates its table arguments before touching a device."""
+    def call(cos=16, sin=16, n_pos=100, pos0=0, style=0, N=8, dt=0, q=16):
+        return lib.fa_fwd_rope(q, 16, 16, 16, None, cos, sin, n_pos, pos0, style, 1, 1, 1, N, 64, 0.1, 0, -1, -1,
+                               dt, dt, 0, None)
+    assert call(cos=None) == fb.FA_ERR_ARG
+    assert call(sin=None) == fb.FA_ERR_ARG
+    assert call(n_pos=0) == fb.FA_ERR_ARG
+    assert call(pos0=-1) == fb.FA_ERR_ARG
+    assert call(pos0=95, N=8) == fb.FA_ERR_ARG          # rows 95 .. 102 run past the 100-entry table
+    assert call(style=2) == fb.FA_ERR_ARG
+    assert call(cos=8) == fb.FA_ERR_ALIGN
+    assert call(dt=2) == fb.FA_ERR_UNSUPPORTED          # the fp32 kernel has no in-kernel rotation
+    assert call(q=None) == fb.FA_ERR_ARG                # then the forward's own checks
