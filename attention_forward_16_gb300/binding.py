@@ -59,6 +59,7 @@ SIGNATURES = {
                          _P]),
     "fa_device_status": (_I, [_P]),
     "fa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
+    "fa_select_fwd_kernel": (_I, [_I]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "fa_plan_units": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), _I]),
     "fa_tile_needs_mask": (_I, [_I, _I, _I, _I, _I, _I]),
@@ -209,6 +210,13 @@ def fa_rope_tables(cos_tab, sin_tab, n_pos, D, base, stream):
 
 def fa_device_status(stream=None):
     return load().fa_device_status(stream)
+
+
+FA_FWD_AUTO, FA_FWD_ONE_CTA, FA_FWD_CTA_PAIR = 0, 1, 2
+
+
+def fa_select_fwd_kernel(which):
+    return load().fa_select_fwd_kernel(which)
 
 
 def fa_set_wait_limit_ns(ns):

@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 
 thread_local char g_last_cuda_err[256] = "no error";
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_fwd_kernel{FA_FWD_AUTO};
 
 __device__ int g_status_word;
 
@@ -77,27 +78,26 @@ int encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     return FA_OK;
 }
 
-// 4-D view of a 16-bit [B, H, N, D] or [B, N, H, D] tensor with the rows (N)
-// as the box's second dimension; box = 128 rows x 64 columns (128 bytes: the
-// widest box the 128-byte swizzle allows).
-int make_map(CUtensorMap* m, const void* base, bool bf16, int layout, int B, int Hx, int N, int D) {
+// 5-D view {64 columns, rows, D / 64 column chunks, heads, batch} of a 16-bit
+// [B, H, N, D] or [B, N, H, D] tensor, so that one TMA instruction moves a
+// whole box of `box_rows` rows x (64 * box_chunks) columns into shared memory
+// as box_chunks blocks of box_rows x 128 bytes (128-byte swizzle), the
+// layout the tensor-core descriptors read.  Whole tiles per instruction
+// matter: a TMA load costs about the same fixed time per instruction up to
+// at least 32 KiB, so two 16 KiB boxes take twice as long as one 32 KiB box.
+int make_tile_map(CUtensorMap* m, const void* base, bool bf16, int layout, int B, int Hx, int N, int D,
+                  int box_rows, int box_chunks) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     int rc = encoder(&enc);
     if (rc != FA_OK) return rc;
     const cuuint64_t e = 2;
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4];
-    if (layout == fa::LAYOUT_BHND) {
-        dims[0] = D; dims[1] = N; dims[2] = Hx; dims[3] = B;
-        strides[0] = (cuuint64_t)D * e; strides[1] = (cuuint64_t)N * D * e; strides[2] = (cuuint64_t)Hx * N * D * e;
-        box[0] = 64; box[1] = fa::kTileM; box[2] = 1; box[3] = 1;
-    } else {
-        dims[0] = D; dims[1] = Hx; dims[2] = N; dims[3] = B;
-        strides[0] = (cuuint64_t)D * e; strides[1] = (cuuint64_t)Hx * D * e; strides[2] = (cuuint64_t)N * Hx * D * e;
-        box[0] = 64; box[1] = 1; box[2] = fa::kTileM; box[3] = 1;
-    }
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+    const cuuint64_t row = layout == fa::LAYOUT_BHND ? (cuuint64_t)D * e : (cuuint64_t)Hx * D * e;
+    const cuuint64_t head = layout == fa::LAYOUT_BHND ? (cuuint64_t)N * D * e : (cuuint64_t)D * e;
+    cuuint64_t dims[5] = {64, (cuuint64_t)N, (cuuint64_t)(D / 64), (cuuint64_t)Hx, (cuuint64_t)B};
+    cuuint64_t strides[4] = {row, 128, head, (cuuint64_t)Hx * N * D * e};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -201,11 +201,21 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     }
 
     const bool bf16 = dtype == FA_BF16;
+    // The one-CTA kernel unless the caller asked for the CTA pair (D = 128).
+    const int sel = g_fwd_kernel.load(std::memory_order_relaxed);
+    const bool pair = D == 128 && sel == FA_FWD_CTA_PAIR && dev->sms >= 2;
     fa::TcParams p;
     std::memset(&p, 0, sizeof(p));
-    if ((rc = make_map(&p.tm_q, q, bf16, layout, B, H, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
+    // Whole tiles per TMA instruction: Q and K/V tiles of 128 rows x D in the
+    // one-CTA kernel; in the pair kernel each CTA's K half is 64 keys x D and
+    // its V half 128 keys x 64 columns (one chunk).
+    const int chunks = D / 64;
+    if ((rc = make_tile_map(&p.tm_q, q, bf16, layout, B, H, N, D, fa::kTileM, chunks)) != FA_OK) return rc;
+    if ((rc = make_tile_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D, pair ? fa::kTileN / 2 : fa::kTileN, chunks)) !=
+        FA_OK)
+        return rc;
+    if ((rc = make_tile_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D, fa::kTileN, pair ? 1 : chunks)) != FA_OK)
+        return rc;
     p.o = o;
     p.lse = lse;
     p.g = g;
@@ -213,7 +223,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     p.H = H;
     p.G = H / H_kv;
     p.layout = layout;
-    const long long units = (long long)BH * fa::n_pairs_for(N);
+    const long long units = (long long)BH * fa::n_pairs_for(N);  // 256 query rows each (both kernels)
     if (units > 0x7fffffffLL) return FA_ERR_ARG;
     p.n_units = (int)units;
     p.order = fa::unit_order_for(g);
@@ -228,8 +238,14 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
         p.rope_style = rope.style;
         p.rope_pos0 = rope.pos0;
     }
-    const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
-    cudaError_t e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
+    cudaError_t e;
+    if (pair) {
+        const int clusters = p.n_units < dev->sms / 2 ? p.n_units : dev->sms / 2;
+        e = fa::launch_tc_pair(p, bf16, scale > 0.f, clusters, s);
+    } else {
+        const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
+        e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
+    }
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
@@ -311,6 +327,11 @@ int fa_device_status(void* stream) {
         return FA_ERR_TIMEOUT;
     }
     return FA_OK;
+}
+
+int fa_select_fwd_kernel(int which) {
+    if (which != FA_FWD_AUTO && which != FA_FWD_ONE_CTA && which != FA_FWD_CTA_PAIR) return FA_ERR_ARG;
+    return g_fwd_kernel.exchange(which);
 }
 
 unsigned long long fa_set_wait_limit_ns(unsigned long long ns) {
@@ -506,10 +527,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     const bool bf16 = dtype == FA_BF16;
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
-    if ((rc = make_map(&p.tm_q, q, bf16, layout, B, H, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D)) != FA_OK) return rc;
-    if ((rc = make_map(&p.tm_do, d_o, bf16, layout, B, H, N, D)) != FA_OK) return rc;
+    const int chunks = D / 64;
+    if ((rc = make_tile_map(&p.tm_q, q, bf16, layout, B, H, N, D, fa::kTileM, chunks)) != FA_OK) return rc;
+    if ((rc = make_tile_map(&p.tm_k, k, bf16, layout, B, H_kv, N, D, fa::kTileN, chunks)) != FA_OK) return rc;
+    if ((rc = make_tile_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D, fa::kTileN, chunks)) != FA_OK) return rc;
+    if ((rc = make_tile_map(&p.tm_do, d_o, bf16, layout, B, H, N, D, fa::kTileM, chunks)) != FA_OK) return rc;
     float* lse2 = static_cast<float*>(workspace);
     float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + vb);
     p.q = q;

@@ -95,18 +95,14 @@ static_assert(BwdCfg<128>::kColDO + 64 <= BwdCfg<128>::kTmemCols && BwdCfg<64>::
 static_assert(dkdv_smem_bytes<128>() <= 227 * 1024 && dq_smem_bytes<128>() <= 227 * 1024, "smem (D=128)");
 static_assert(dkdv_smem_bytes<64>() <= 227 * 1024 && dq_smem_bytes<64>() <= 227 * 1024, "smem (D=64)");
 
-// 4-D tensor-map load of one 128-row tile (all D columns): coordinates
-// (d, row, head, batch), rows and heads swapped for [B, N, H, D].
+// One 128-row tile (all D columns, as D/64 swizzled 128-byte-wide blocks) in
+// one TMA instruction: the 5-D map's coordinates are (column, row, chunk,
+// head, batch) in either layout.
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int layout, int b,
                                           int head, int row) {
-#pragma unroll
-    for (int c = 0; c < BwdCfg<D>::kChunks; ++c) {
-        if (layout == LAYOUT_BHND)
-            tma_load_4d(dst + c * BwdCfg<D>::kBoxBytes, tm, bar, c * 64, row, head, b);
-        else
-            tma_load_4d(dst + c * BwdCfg<D>::kBoxBytes, tm, bar, c * 64, head, row, b);
-    }
+    (void)layout;
+    tma_load_5d(dst, tm, bar, 0, row, 0, head, b);
 }
 
 // Products shared by both kernels.  A tiles are K-major 128 x D (TMA boxes

@@ -141,8 +141,16 @@ struct Unit {
 
 FA_HD int n_pairs_for(int N) { return (N + 2 * kTileM - 1) / (2 * kTileM); }
 
-FA_HD Unit make_unit(const Geom& g, int BH, int order, int u) {
-    const int np = n_pairs_for(g.N);
+// Units of the CTA-pair kernel: four 128-row Q tiles, two 256-row slots.
+// Slot t covers rows [q0 + 256 t, q0 + 256 t + 256): its first 128 rows sit
+// in the pair's first CTA and the next 128 in the second, and one M = 256
+// product serves both, so both visit every key tile any of the 256 rows needs.
+constexpr int kSlotRowsPair = 2 * kTileM;
+FA_HD int n_quads_for(int N) { return (N + 2 * kSlotRowsPair - 1) / (2 * kSlotRowsPair); }
+
+// Unit u in enumeration order `order`, with slots of `slot_rows` query rows.
+FA_HD Unit make_unit_rows(const Geom& g, int BH, int order, int u, int slot_rows) {
+    const int np = (g.N + 2 * slot_rows - 1) / (2 * slot_rows);
     int bh, pair;
     if (order == ORDER_HEAD_MAJOR) {
         bh = u / np;
@@ -156,21 +164,32 @@ FA_HD Unit make_unit(const Geom& g, int BH, int order, int u) {
     }
     Unit un;
     un.bh = bh;
-    un.q0 = pair * 2 * kTileM;
+    un.q0 = pair * 2 * slot_rows;
     un.jlo = 0x7fffffff;
     un.jhi = 0;
     for (int t = 0; t < 2; ++t) {
-        int r0 = un.q0 + t * kTileM;
+        int r0 = un.q0 + t * slot_rows;
         if (r0 >= g.N) {
             un.lo[t] = un.hi[t] = 0;
             continue;
         }
-        int r1 = r0 + kTileM < g.N ? r0 + kTileM : g.N;
+        int r1 = r0 + slot_rows < g.N ? r0 + slot_rows : g.N;
         kv_tile_range(g, r0, r1, un.lo[t], un.hi[t]);
         if (un.lo[t] < un.jlo) un.jlo = un.lo[t];
         if (un.hi[t] > un.jhi) un.jhi = un.hi[t];
     }
     return un;
+}
+
+FA_HD Unit make_unit(const Geom& g, int BH, int order, int u) { return make_unit_rows(g, BH, order, u, kTileM); }
+FA_HD Unit make_unit_pair(const Geom& g, int BH, int order, int u) {
+    return make_unit_rows(g, BH, order, u, kSlotRowsPair);
+}
+
+// bf16 split of P for a 256-row slot of the pair kernel: both CTAs take the
+// same decision (one product reads both halves), split if either half needs it.
+FA_HD bool slot_split_p(const Geom& g, int r0) {
+    return tile_split_p(g, r0) || tile_split_p(g, r0 + kTileM);
 }
 
 // The unit a persistent CTA takes in round r: rounds hand out `ctas`

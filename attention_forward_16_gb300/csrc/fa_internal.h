@@ -22,9 +22,9 @@ FA_HD long long row_index(int layout, int b, int h, int i, int H, int N) {
 }
 
 struct TcParams {
-    CUtensorMap tm_q;   // 4-D maps: {D, N, H, B} ([B,H,N,D]) or {D, H, N, B} ([B,N,H,D]);
-    CUtensorMap tm_k;   // 16-bit, box of 128 rows x 64 columns, 128-byte swizzle
-    CUtensorMap tm_v;
+    CUtensorMap tm_q;   // 5-D maps {64 columns, rows, D/64 chunks, heads, batch} of either layout,
+    CUtensorMap tm_k;   // 16-bit, 128-byte swizzle; one box is a whole tile (all chunks of
+    CUtensorMap tm_v;   // 128 rows; the pair kernel's K and V halves: see launch_tc_pair)
     void* o;            // O in Q's layout, 16-bit or fp32 (o_f32)
     float* lse;         // [B, H, N] or null
     Geom g;
@@ -140,7 +140,7 @@ inline unsigned long long decode_workspace_bytes(long long BH, int Nq, int D, in
 // Backward pass (dQ, dK, dV).  Rows are padded to a whole number of 128-row
 // tiles in the per-row vectors so the kernels copy them without tail checks.
 struct BwdParams {
-    CUtensorMap tm_q;   // 4-D maps as in TcParams: Q and dO with H heads,
+    CUtensorMap tm_q;   // whole-tile 5-D maps as in TcParams: Q and dO with H heads,
     CUtensorMap tm_k;   // K and V with H_kv heads
     CUtensorMap tm_v;
     CUtensorMap tm_do;
@@ -191,6 +191,10 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype_code, cudaStream_t s)
 // head) select, at head dimension D (0 if the runtime cannot say).
 int decode_ctas_per_sm(int rows, int D);
 cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s);
+// The CTA-pair forward (D = 128): `clusters` persistent 2-CTA clusters over
+// p.n_units 256-row units; tm_k's box is 64 keys x 128 columns (one CTA's
+// half of a K tile), tm_v's 128 keys x 64 columns (half of a V tile).
+cudaError_t launch_tc_pair(const TcParams& p, bool bf16, bool pos_scale, int clusters, cudaStream_t s);
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, float* lse2, float* dsum, int B,
                            int H, int N, int Npad, int D, int layout, int dtype_code, int sms, cudaStream_t s);

@@ -100,14 +100,12 @@ static_assert(TcCfg<128>::kStages >= 4 && TcCfg<64>::kStages >= 4, "K/V ring too
 static_assert(smem_bytes<64>() <= 227 * 1024, "shared memory budget (D=64)");
 
 // ------------------------------------------------------------ TMA producers
-// Tensor-map coordinates (d, row, head, batch) of a 128-row x 64-column box;
-// rows and heads trade places for [B, N, H, D].
-__device__ __forceinline__ void load_box(const TcParams& p, uint32_t dst, const CUtensorMap* tm, uint32_t bar, int c,
-                                         int row, int head, int b) {
-    if (p.layout == LAYOUT_BHND)
-        tma_load_4d(dst, tm, bar, c * 64, row, head, b);
-    else
-        tma_load_4d(dst, tm, bar, c * 64, head, row, b);
+// One whole tile (128 rows x D, all column chunks) in one TMA instruction:
+// the 5-D map's coordinates are (column, row, chunk, head, batch) in either
+// layout.
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int row, int head,
+                                          int b) {
+    tma_load_5d(dst, tm, bar, 0, row, 0, head, b);
 }
 
 // Q tiles: one thread, one buffer per tile.  Tile t of the next unit is loaded
@@ -128,8 +126,7 @@ __device__ __forceinline__ void tma_q_role(const TcParams& p, const Waiter& W, S
             const uint32_t q_full = smem_u32(&sh->q_full[t]);
             if (q_it[t] > 0 && !(ok = W.wait(smem_u32(&sh->q_empty[t]), (q_it[t] - 1) & 1))) break;
             mbar_arrive_expect_tx(q_full, C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                load_box(p, sQa + t * C::kTileBytes + c * C::kBoxBytes, &p.tm_q, q_full, c, un.q0 + t * kTileM, h, b);
+            load_tile(sQa + t * C::kTileBytes, &p.tm_q, q_full, un.q0 + t * kTileM, h, b);
             ++q_it[t];
         }
         // Pull this CTA's next Q tiles into L2 now: their loads wait for this
@@ -138,13 +135,7 @@ __device__ __forceinline__ void tma_q_role(const TcParams& p, const Waiter& W, S
         if (ok && un_next < p.n_units) {
             const Unit nx = make_unit(p.g, p.BH, p.order, un_next);
             const int nb = nx.bh / p.H, nh = nx.bh % p.H;
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < C::kChunks; ++c) {
-                    if (p.layout == LAYOUT_BHND)
-                        tma_prefetch_l2_4d(&p.tm_q, c * 64, nx.q0 + t * kTileM, nh, nb);
-                    else
-                        tma_prefetch_l2_4d(&p.tm_q, c * 64, nh, nx.q0 + t * kTileM, nb);
-                }
+            for (int t = 0; t < 2; ++t) tma_prefetch_l2_5d(&p.tm_q, 0, nx.q0 + t * kTileM, 0, nh, nb);
         }
     }
     // Let every issued copy land before shared memory is released (on the
@@ -174,8 +165,7 @@ __device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, 
                 const uint32_t full = smem_u32(&sh->kv_full[slot]);
                 mbar_arrive_expect_tx(full, C::kTileBytes);
                 const CUtensorMap* tm = kv ? &p.tm_v : &p.tm_k;
-                for (int c = 0; c < C::kChunks; ++c)
-                    load_box(p, sKVa + slot * C::kTileBytes + c * C::kBoxBytes, tm, full, c, j * kTileN, hk, b);
+                load_tile(sKVa + slot * C::kTileBytes, tm, full, j * kTileN, hk, b);
                 ++kv_it;
             }
         }

@@ -79,6 +79,58 @@ struct Waiter {
     }
 };
 
+// Bounded waits for a CTA pair: a timeout also raises the other CTA's abort
+// flag (written through its shared-memory window) so both halves of the pair
+// stop promptly.
+struct PairWaiter {
+    volatile int* abort;       // this CTA's flag
+    volatile int* peer_abort;  // the other CTA's flag
+    int* status;
+    unsigned long long limit;
+
+    __device__ __forceinline__ void raise() const {
+        *abort = 1;
+        *peer_abort = 1;
+        atomicExch(status, DEV_TIMEOUT);
+    }
+    // kCluster: acquire at cluster scope, for barriers that take arrivals
+    // from threads of the other CTA; barriers signalled by this CTA's threads,
+    // by tcgen05.commit or by TMA completion need only CTA scope.
+    template <bool kCluster = false>
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        auto probe = [&] { return kCluster ? mbar_try_wait_cl(bar, parity) : mbar_try_wait_nohint(bar, parity); };
+        if (probe()) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (probe()) return true;
+            if ((it & 15u) == 0) {
+                if (*abort) return false;
+                if (globaltimer_ns() - t0 > limit) {
+                    raise();
+                    return false;
+                }
+            }
+        }
+    }
+    template <bool kCluster = false>
+    __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) const {
+        bool ok = wait<kCluster>(bar, parity);
+        return __all_sync(0xffffffffu, ok);
+    }
+    // Exit-time wait for issued asynchronous work, ignoring the abort flag,
+    // bounded by Waiter::kDrainLimitNs from `t0` (one deadline for a whole
+    // sequence of drains) or the ordinary limit if that is longer.
+    __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, uint64_t t0) const {
+        const unsigned long long bound = limit > Waiter::kDrainLimitNs ? limit : Waiter::kDrainLimitNs;
+        while (!mbar_try_wait_cl_hint(bar, parity)) {
+            if (globaltimer_ns() - t0 > bound) {
+                atomicExch(status, DEV_TIMEOUT);
+                return;
+            }
+        }
+    }
+};
+
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 

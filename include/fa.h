@@ -384,6 +384,27 @@ int fa_rope_tables(float* cos_tab, float* sin_tab, int n_pos, int D, double base
  */
 int fa_device_status(void* stream);
 
+/* Forward kernels (fa_select_fwd_kernel). */
+enum {
+    FA_FWD_AUTO = 0,      /* the one-CTA kernel (measured the faster of the two on every benchmark shape) */
+    FA_FWD_ONE_CTA = 1,   /* one CTA per SM, two 128-row Q tiles, M = 128 products */
+    FA_FWD_CTA_PAIR = 2   /* 2-CTA clusters, M = 256 products over an SM pair (D = 128 only;
+                             other head sizes still take the one-CTA kernel) */
+};
+
+/*
+ * fa_select_fwd_kernel -- choose the tensor-core forward kernel that later
+ * fa_fwd* / fa_fwd_gqa / fa_fwd_rope calls launch (process-wide; default
+ * FA_FWD_AUTO).  Both compute the same result by the same method; they
+ * differ in how work maps onto SMs.  The one-CTA kernel runs one CTA per SM
+ * with two 128-row query tiles and M = 128 tcgen05 products.  The CTA-pair
+ * kernel runs 2-CTA clusters whose M = 256 products
+ * (tcgen05.mma.cta_group::2) split every K and V tile between the two SMs,
+ * halving the per-SM shared-memory traffic.  Returns the previous choice, or
+ * FA_ERR_ARG for an unknown value.  Host-only.
+ */
+int fa_select_fwd_kernel(int which);
+
 /* Smallest wait limit fa_set_wait_limit_ns accepts, in nanoseconds. */
 #define FA_MIN_WAIT_LIMIT_NS 1000ull
 

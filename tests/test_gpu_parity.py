@@ -281,18 +281,22 @@ def test_watchdog_reports_timeout_and_context_survives():
     _check(o, lse, ro, rlse, "f16", True, "after watchdog")
 
 
+@pytest.mark.parametrize("kernel", ["one_cta", "cta_pair"])
 @pytest.mark.parametrize("dtype,mk", [("f16", MASK_NONE), ("bf16", MASK_CAUSAL)])
-def test_forward_kernel_waits_run_out_and_context_survives(dtype, mk):
+def test_forward_kernel_waits_run_out_and_context_survives(dtype, mk, kernel):
     """The attention kernel's own bounded waits, not a separate probe: with the
     limit at its 1 us floor, the first wait for a Q or K/V tile from HBM (or
     for the first S) outlasts it, so every CTA records a timeout, stops, lets
     the copies and products it issued land (the exit drain keeps its own 1 s
-    bound), frees TMEM and returns.  The host reads FA_ERR_TIMEOUT; with the
-    limit restored, the next call on the same context passes parity."""
+    bound), frees TMEM and returns; in the 2-CTA kernel a timeout in either
+    CTA stops both, and the pair frees TMEM together once the first CTA's
+    products have drained.  The host reads FA_ERR_TIMEOUT; with the limit
+    restored, the next call on the same context passes parity."""
     q, k, v = make_qkv(2, 16, 2048, 128, dtype, seed=16)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     causal = mk == MASK_CAUSAL
     assert fb.fa_device_status(None) == 0
+    sel = fb.fa_select_fwd_kernel(fb.FA_FWD_CTA_PAIR if kernel == "cta_pair" else fb.FA_FWD_ONE_CTA)
     prev = fb.fa_set_wait_limit_ns(1)          # raised to the 1 us floor
     try:
         fa.attention_fwd(dq, dk, dv, causal=causal)   # outputs undefined: the launch is cut short
@@ -300,6 +304,7 @@ def test_forward_kernel_waits_run_out_and_context_survives(dtype, mk):
         rc = fb.fa_device_status(None)
     finally:
         assert fb.fa_set_wait_limit_ns(prev) == 1000
+        fb.fa_select_fwd_kernel(sel)
     assert rc == fb.FA_ERR_TIMEOUT
     assert fb.fa_device_status(None) == 0       # cleared by the read
     q2, k2, v2 = (t[:, :2].contiguous() for t in (q, k, v))
@@ -495,3 +500,78 @@ def test_long_sequences_sampled_rows(dtype, D, N, mk, wl, wr):
                                             wl, wr, q_offset=r0)
             _check(o[:, h:h + 1, r0:r0 + 64].astype(np.float64), lse[:, h:h + 1, r0:r0 + 64].astype(np.float64),
                    ro, rlse, dtype, False, f"N={N} head {h} rows {r0}..")
+
+
+# ------------------------------------------------- the CTA-pair forward kernel
+
+@pytest.fixture
+def pair_kernel():
+    prev = fb.fa_select_fwd_kernel(fb.FA_FWD_CTA_PAIR)
+    yield
+    fb.fa_select_fwd_kernel(prev)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 7, 128, 129, 255, 256, 640, 1000])
+def test_pair_kernel_ragged_all_masks(pair_kernel, dtype, N):
+    """The 2-CTA kernel (M = 256 products over an SM pair, each CTA holding
+    half of every K and V tile, three S buffers) meets the same bounds on
+    ragged lengths and every mask, with O in fp32 and in the input type."""
+    q, k, v = make_qkv(2, 3, N, 128, dtype, seed=9000 + N)
+    for mk, wl, wr in MASK_SET:
+        for o_f32 in (True, False):
+            o, lse = _run(q, k, v, 0.088, mk, wl, wr, o_f32)
+            ro, rlse = _ref(q, k, v, 0.088, mk, wl, wr)
+            _check(o, lse, ro, rlse, dtype, o_f32, f"pair {dtype} N={N} mask={mk},{wl},{wr} o_f32={o_f32}")
+
+
+@pytest.mark.parametrize("name", ["f16_full_4k", "bf16_causal_4k", "bf16_window_16k"])
+def test_pair_kernel_full_size_raw_bound(pair_kernel, name):
+    """Benchmark shapes on the 2-CTA kernel, fp32 O, raw bounds on sampled
+    heads and row blocks (the first rows, where |O| is largest, included)."""
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    window = (w.win_l, w.win_r) if w.mask == MASK_WINDOW else None
+    o, lse = fa.attention_fwd(q.cuda(), k.cuda(), v.cuda(), scale=w.scale, causal=w.mask == MASK_CAUSAL,
+                              window=window, o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    o = o.cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    for b, h, r0, r1 in ((0, 0, 0, 512), (w.B - 1, w.H - 1, w.N - 512, w.N), (w.B // 2, w.H // 2, 1000, 1512)):
+        ro, rlse = attention_three_pass(qd[b:b + 1, h:h + 1, r0:r1], kd[b:b + 1, h:h + 1], vd[b:b + 1, h:h + 1],
+                                        w.scale, w.mask, w.win_l, w.win_r, q_offset=r0)
+        assert np.abs(o[b, h, r0:r1] - ro[0, 0]).max() <= TOL_O_16, (name, b, h, r0)
+        assert np.abs(lse[b, h, r0:r1] - rlse[0, 0]).max() <= TOL_LSE_16, (name, b, h, r0)
+
+
+def test_pair_kernel_layouts_gqa_and_rope(pair_kernel):
+    """[B, N, H, D] input and grouped K/V heads on the 2-CTA kernel against the
+    oracle, and the rotary embedding of Q (rotated by that kernel's Q-release
+    warps) bit-equal to the two-pass path."""
+    from oracle import attention_grouped
+    B, H, Hkv, N, D = 2, 4, 2, 300, 128
+    q, _, _ = make_qkv(B, H, N, D, "bf16", seed=77)
+    _, k, v = make_qkv(B, Hkv, N, D, "bf16", seed=78)
+    qb, kb, vb = (t.permute(0, 2, 1, 3).contiguous().cuda() for t in (q, k, v))
+    o, lse = fa.attention_fwd(qb, kb, vb, causal=True, layout="bnhd", o_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rlse = attention_grouped(q.double().numpy(), k.double().numpy(), v.double().numpy(), 1 / math.sqrt(D),
+                                 MASK_CAUSAL)
+    _check(o.cpu().permute(0, 2, 1, 3).numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rlse,
+           "bf16", True, "pair bnhd gqa")
+    cos, sin = fa.rope_tables(N + 9, D, 10000.0)
+    _, kr = fa.apply_rope(None, kb, cos, sin, k_pos0=9, layout="bnhd")
+    qr, _ = fa.apply_rope(qb, None, cos, sin, q_pos0=9, layout="bnhd")
+    o1, l1 = fa.attention_fwd(qb, kr, vb, layout="bnhd", rope=(cos, sin), rope_pos0=9)
+    o2, l2 = fa.attention_fwd(qr, kr, vb, layout="bnhd")
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_kernel_selector_rejects_unknown_values():
+    assert fb.fa_select_fwd_kernel(7) == fb.FA_ERR_ARG
+    prev = fb.fa_select_fwd_kernel(fb.FA_FWD_AUTO)
+    assert fb.fa_select_fwd_kernel(prev) == fb.FA_FWD_AUTO

@@ -302,3 +302,16 @@ def test_fwd_rope_rejections_before_any_launch(lib):
     assert call(cos=8) == fb.FA_ERR_ALIGN
     assert call(dt=2) == fb.FA_ERR_UNSUPPORTED          # the fp32 kernel has no in-kernel rotation
     assert call(q=None) == fb.FA_ERR_ARG                # then the forward's own checks
+
+
+def test_forward_kernel_selector_is_host_only(lib):
+    """fa_select_fwd_kernel only records the choice (no device needed) and
+    refuses values that name no kernel."""
+    prev = lib.fa_select_fwd_kernel(fb.FA_FWD_CTA_PAIR)
+    try:
+        assert lib.fa_select_fwd_kernel(fb.FA_FWD_ONE_CTA) == fb.FA_FWD_CTA_PAIR
+        assert lib.fa_select_fwd_kernel(3) == fb.FA_ERR_ARG
+        assert lib.fa_select_fwd_kernel(-1) == fb.FA_ERR_ARG
+        assert lib.fa_select_fwd_kernel(fb.FA_FWD_AUTO) == fb.FA_FWD_ONE_CTA
+    finally:
+        lib.fa_select_fwd_kernel(prev)
