@@ -40,6 +40,7 @@
 #include "ptx.cuh"
 #include "rope_math.cuh"
 #include "tc_common.cuh"
+#include "tc_softmax.cuh"
 
 namespace fa {
 namespace {
@@ -59,8 +60,6 @@ constexpr int kWarpMma = 8;    // MMA issuer for Q tile 0; TMEM owner
 constexpr int kWarpTma = 9;
 constexpr int kWarpMma1 = 10;  // MMA issuer for Q tile 1
 constexpr int kWarpTmaQ = 11;  // Q tile loads
-constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
-constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
 struct TcCfg {
@@ -353,61 +352,6 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     W.drain(drain, 0);
 }
 
-// ------------------------------------------- rotary embedding of a Q tile
-// One query row of a Q tile in shared memory, rotated in place by the table
-// entries of its position (the rotation of "Ascend C advanced practice:
-// high-performance FlashAttention-2-style tile-level fused attention",
-// section 9, applied to Q as it is loaded; K arrives already rotated).  The
-// tile holds D/64 column chunks of 128 rows x 128 bytes, 128-byte swizzled:
-// 16-byte unit U of row r sits at chunk U/8, slot (U%8) ^ (r%8).  Groups of
-// eight pairs: half-split pairs units g and D/16 + g element by element,
-// interleaved pairs neighbours inside units 2g and 2g + 1.
-template <int D, bool kBf16>
-__device__ __forceinline__ void rope_q_row(uint8_t* tile, int row, const float* cos_row, const float* sin_row,
-                                           int style) {
-    constexpr int kBox = TcCfg<D>::kBoxBytes;
-    uint8_t* rb = tile + row * 128;
-    const int sw = row & 7;
-#pragma unroll
-    for (int g = 0; g < D / 16; ++g) {
-        const float4 c0 = __ldg(reinterpret_cast<const float4*>(cos_row + 8 * g));
-        const float4 c1 = __ldg(reinterpret_cast<const float4*>(cos_row + 8 * g + 4));
-        const float4 s0 = __ldg(reinterpret_cast<const float4*>(sin_row + 8 * g));
-        const float4 s1 = __ldg(reinterpret_cast<const float4*>(sin_row + 8 * g + 4));
-        const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const int ua = style == ROPE_HALF ? g : 2 * g;
-        const int ub = style == ROPE_HALF ? D / 16 + g : 2 * g + 1;
-        uint4* pa = reinterpret_cast<uint4*>(rb + (ua >> 3) * kBox + (((ua & 7) ^ sw) << 4));
-        uint4* pb = reinterpret_cast<uint4*>(rb + (ub >> 3) * kBox + (((ub & 7) ^ sw) << 4));
-        const uint4 wa = *pa, wb = *pb;
-        const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
-        const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
-        float u[8], v[8], yu[8], yv[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            u[2 * i] = lo_half<kBf16>(xa[i]);
-            u[2 * i + 1] = hi_half<kBf16>(xa[i]);
-            v[2 * i] = lo_half<kBf16>(xb[i]);
-            v[2 * i + 1] = hi_half<kBf16>(xb[i]);
-        }
-        if (style == ROPE_HALF) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) rope_rotate(u[m], v[m], c[m], sn[m], yu[m], yv[m]);
-        } else {
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                rope_rotate(u[2 * m], u[2 * m + 1], c[m], sn[m], yu[2 * m], yu[2 * m + 1]);
-                rope_rotate(v[2 * m], v[2 * m + 1], c[4 + m], sn[4 + m], yv[2 * m], yv[2 * m + 1]);
-            }
-        }
-        *pa = make_uint4(pack2<kBf16>(yu[0], yu[1]), pack2<kBf16>(yu[2], yu[3]), pack2<kBf16>(yu[4], yu[5]),
-                         pack2<kBf16>(yu[6], yu[7]));
-        *pb = make_uint4(pack2<kBf16>(yv[0], yv[1]), pack2<kBf16>(yv[2], yv[3]), pack2<kBf16>(yv[4], yv[5]),
-                         pack2<kBf16>(yv[6], yv[7]));
-    }
-}
-
 // ------------------------------------------------------ softmax + epilogue
 template <int D, bool kBf16, bool kPosScale>
 __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t tmem,
@@ -440,7 +384,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             ++q_cnt;
             if (jlo_t < jhi_t && qi < p.g.N) {
                 const long long pos = (long long)p.rope_pos0 + qi;
-                rope_q_row<D, kBf16>(sQ + t * C::kTileBytes, row, p.rope_cos + pos * (D / 2),
+                rope_q_row<D, kBf16, C::kBoxBytes>(sQ + t * C::kTileBytes, row, p.rope_cos + pos * (D / 2),
                                      p.rope_sin + pos * (D / 2), p.rope_style);
             }
             fence_proxy_async_smem();
@@ -454,122 +398,10 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             if (!(ok = W.wait_warp(s_full, s_cnt & 1))) break;
             ++s_cnt;
             tc_fence_after();
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
-            tmem_wait_ld();
-
-            if (!kPosScale) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float a, b;
-                        fmul2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), c2, c2);
-                        s[c][i] = f2u(a);
-                        s[c][i + 1] = f2u(b);
-                    }
-            }
-            if (tile_needs_mask(p.g, r0, j)) {
-                int c_lo, c_hi;
-                row_visible_cols(p.g, qi, j, c_lo, c_hi);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = c * 32 + i;
-                        if (col < c_lo || col > c_hi) s[c][i] = f2u(-INFINITY);
-                    }
-            }
-            // Row max: 64 three-input maxes spread over 8 independent chains.
-            float mxk[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(u2f(s[0][2 * k]), u2f(s[0][2 * k + 1]));
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = (c == 0 ? 16 : 0); i < 32; i += 2) {
-                    const int k = (i >> 1) & 7;
-                    mxk[k] = max3(mxk[k], u2f(s[c][i]), u2f(s[c][i + 1]));
-                }
-            const float mx = fmaxf(max3(mxk[0], mxk[1], mxk[2]), max3(max3(mxk[3], mxk[4], mxk[5]), mxk[6], mxk[7]));
-            const float m_new = kPosScale ? mx * c2 : mx;
-
-            const bool first = j == jlo_t;
-            float alpha = 1.f;
-            bool resc = false;
-            if (first) {
-                m_ref = m_new;
-            } else if (m_new > m_ref + kTau) {
-                alpha = ex2(m_ref - m_new);
-                m_ref = m_new;
-                resc = true;
-            }
-            l *= alpha;
-            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-            float l0 = 0.f, l1 = 0.f;
-            if (!split) {
-                // p = 2^(s*c - m) two at a time (packed FFMA, two ex2), packed into
-                // 16-bit pairs; the row sum runs over four packed accumulators.
-                float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float a, b;
-                        if (kPosScale)
-                            ffma2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), c2, c2, neg_m, neg_m);
-                        else
-                            fadd2(a, b, u2f(s[c][i]), u2f(s[c][i + 1]), neg_m, neg_m);
-                        a = ex2(a);
-                        b = ex2(b);
-                        pk[i >> 1] = pack2<kBf16>(a, b);
-                        const int k = (i >> 1) & 3;
-                        fadd2(acc[k][0], acc[k][1], acc[k][0], acc[k][1], a, b);
-                    }
-                    tmem_st16(tS + 16 * c, pk);
-                }
-                l0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
-                l1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
-            } else {
-                // p = hi + lo, both bf16: hi in columns [0, 64), lo in [64, 128).
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t hw[16], lw[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float a = kPosScale ? ex2(fmaf(u2f(s[c][i]), c2, neg_m)) : ex2(u2f(s[c][i]) + neg_m);
-                        const float b =
-                            kPosScale ? ex2(fmaf(u2f(s[c][i + 1]), c2, neg_m)) : ex2(u2f(s[c][i + 1]) + neg_m);
-                        const uint32_t w = pack2<kBf16>(a, b);
-                        hw[i >> 1] = w;
-                        lw[i >> 1] = pack2<kBf16>(a - lo_half<kBf16>(w), b - hi_half<kBf16>(w));
-                        l0 += a;
-                        l1 += b;
-                    }
-                    tmem_st16(tS + c * 16, hw);
-                    tmem_st16(tS + 64 + c * 16, lw);
-                }
-            }
-            if (!first && __any_sync(0xffffffffu, resc)) {
-                // Rare: the running max moved by more than kTau; rescale this row of O.
-                // O is stable here: the MMA that wrote it completed before S_j did, and
-                // the next P.V waits for this warpgroup's arrival below.
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                    tmem_st32(tO + c * 32, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
+            float lsum;
+            softmax_tile<D, kBf16, kPosScale>(p.g, tS, tO, c2, r0, qi, j, j == jlo_t, split, m_ref, l, lsum);
             mbar_arrive(p_full);
-            l += l0 + l1;
+            l += lsum;
         }
         if (!ok) break;
 

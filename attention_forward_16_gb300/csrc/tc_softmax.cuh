@@ -76,7 +76,7 @@ __device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_
     const float mx = fmaxf(max3(mxk[0], mxk[1], mxk[2]), max3(max3(mxk[3], mxk[4], mxk[5]), mxk[6], mxk[7]));
     const float m_new = kPosScale ? mx * c2 : mx;
 
-                float alpha = 1.f;
+    float alpha = 1.f;
     bool resc = false;
     if (first) {
         m_ref = m_new;
