@@ -20,15 +20,17 @@
 //
 // The launch gives 168 registers a thread (12 warps, three per SM
 // sub-partition); setmaxnreg then moves 48 from the MMA/TMA warpgroup to the
-// softmax warpgroups, so a softmax thread can hold its 128-score row
+// softmax warpgroups, for their 64 scores a row plus the epilogue's O chunk
 // (192 + 192 + 120 = 3 x 168).
 //
-// TMEM (512 columns x 128 lanes x 32 bit): S0 | S1 | O0 | O1.  P (16-bit)
-// overwrites the first half of its S columns and feeds the P.V MMA straight
-// from TMEM.  The two softmax warpgroups ping-pong: while one turns S into P,
-// the tensor core runs the other tile's MMAs.  Each tile has its own issuing
-// warp (order P.V(j), S(j+1) per tile), and the two take turns on the tensor
-// core.
+// TMEM (512 columns x 128 lanes x 32 bit): S0 | S1 | O0 | O1.  Each S holds
+// a 128-key tile as two 64-key halves with their own barriers, and the
+// softmax takes each half as an online-softmax step of its own.  P (16-bit)
+// overwrites the first half of its S half's columns and feeds the P.V MMA
+// straight from TMEM.  Splitting S in two gives every Q tile a second S
+// buffer inside the same 512 columns: while a softmax warpgroup turns one
+// half into P, the tensor core computes the other half's S or the other Q
+// tile's products, so the softmax never waits for its own tile's MMAs.
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records a
 // timeout in the device status word, lets its in-flight copies and MMAs
@@ -79,9 +81,10 @@ struct __align__(16) SharedCtl {
     uint64_t q_full[2], q_empty[2];  // per Q tile
     uint64_t q_ready[2];             // per Q tile: rotated in place (rotary embedding of Q)
     uint64_t kv_full[8], kv_empty[8];
-    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t s_full[2][2], p_full[2][2];  // per Q tile and S half
+    uint64_t pv_done[2][2];               // per Q tile: P.V products completed, by step parity
+    uint64_t o_done[2], o_free[2];
     uint64_t drain[2];
-    unsigned long long progress[2];  // per tile: (unit sequence << 32) | (last issued key step + 1)
     uint32_t tmem_base;
     int abort;
 };
@@ -177,12 +180,18 @@ __device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, 
 }
 
 // -------------------------------------------------------------- MMA issuers
-// One issuing warp per Q tile t: S_t(j) = Q_t K_j^T and O_t += P_t(j) V_j.
-// Each warp keeps its own tile's order (S_t(j+1) after P.V_t(j), since P
-// aliases S).  A K/V ring slot is released once both warps have arrived
-// (count 2); a tile with no work on key tile j still waits for that slot to
-// be full before arriving, which keeps the phases of the ring aligned.  Each
-// Q tile's buffer is released by its own warp once its last S has completed.
+// One issuing warp per Q tile t.  Each 128-key tile j is taken in two halves
+// of 64 keys, each with its own S columns: S_t,h(j) = Q_t K_j[64h, 64h+64)^T
+// and O_t += P_t,h(j) V_j[64h, 64h+64).  P_t,h overwrites S_t,h, so the next
+// S_t,h waits for the P.V that reads it, but the other half's S is already
+// computed: the softmax of one half runs while the tensor core works on the
+// other half (of this tile or of the other Q tile), and no step of the softmax
+// waits for its own tile's MMAs.  Issue order per tile:
+//   S(lo,0) S(lo,1) | PV(j,0) S(j+1,0) PV(j,1) S(j+1,1) | ...
+// A K/V ring slot is released once both warps have arrived (count 2); a tile
+// with no work on key tile j still waits for that slot to be full before
+// arriving, which keeps the phases of the ring aligned.  Each Q tile's buffer
+// is released by its own warp once its last S has completed.
 //
 // The whole warp runs this role on one path: every wait, counter and shared-
 // memory descriptor is warp-uniform, and one elected lane issues the
@@ -197,13 +206,12 @@ template <int D, bool kBf16>
 __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
                                          uint32_t sKVa, uint32_t tmem, int t) {
     using C = TcCfg<D>;
-    constexpr uint32_t idesc_s = make_idesc(kBf16, kTileM, kTileN, false);
+    constexpr int kHalf = kTileN / 2;
+    constexpr uint32_t idesc_s = make_idesc(kBf16, kTileM, kHalf, false);
     constexpr uint32_t idesc_o = make_idesc(kBf16, kTileM, D, true);
     const uint32_t dS = tmem + (t ? C::kColS1 : C::kColS0);
     const uint32_t dO = tmem + (t ? C::kColO1 : C::kColO0);
     const uint32_t qa = sQa + t * C::kTileBytes;
-    const uint32_t s_full = smem_u32(&sh->s_full[t]);
-    const uint32_t p_full = smem_u32(&sh->p_full[t]);
     const uint32_t o_done = smem_u32(&sh->o_done[t]);
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
     // With the rotary embedding of Q the tile is released to this warp by its
@@ -211,72 +219,45 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     const uint32_t q_full = smem_u32(p.rope ? &sh->q_ready[t] : &sh->q_full[t]);
     const uint32_t q_empty = smem_u32(&sh->q_empty[t]);
     const bool leader = elect_one();
-    uint32_t kv_it = 0, q_it = 0, p_cnt = 0, o_cnt = 0;
+    uint32_t kv_it = 0, q_it = 0, o_cnt = 0, pv_it = 0;
+    uint32_t p_cnt[2] = {0, 0};
     bool ok = true;
-    volatile unsigned long long* my_progress = &sh->progress[t];
-    volatile unsigned long long* other_progress = &sh->progress[1 - t];
-    // The two issuers alternate on the tensor core: tile 1 issues key step j
-    // only after tile 0 has, and tile 0 issues step j only after tile 1 has
-    // issued step j - 1.  Each warp still wakes on its own P, so neither
-    // tile's P waits behind the other tile's MMA issue, and the two softmaxes
-    // stay half a step apart instead of competing for the same cycles.
-    auto publish = [&](unsigned long long v) {
-        if (leader) *my_progress = v;
-    };
-    auto wait_turn = [&](unsigned long long target) {
-        bool r = true;
-        if (*other_progress < target) {
-            const uint64_t t0 = globaltimer_ns();
-            for (uint32_t it = 1;; ++it) {
-                if (*other_progress >= target) break;
-                if ((it & 15u) == 0) {
-                    if (*W.abort) {
-                        r = false;
-                        break;
-                    }
-                    if (globaltimer_ns() - t0 > W.limit) {
-                        *W.abort = 1;
-                        atomicExch(W.status, DEV_TIMEOUT);
-                        r = false;
-                        break;
-                    }
-                }
-            }
-        }
-        return __all_sync(0xffffffffu, r);
-    };
 
-    // S = Q K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row).
+    // S = Q K^T: K = D in steps of 16 (32 bytes inside a 128-byte swizzled row);
+    // half h starts 64 key rows (8 swizzle atoms) into each column chunk of K.
     const uint64_t q_desc = make_sdesc(qa, 16, 1024);
     const uint64_t k_desc = make_sdesc(sKVa, 16, 1024);
     const uint64_t v_desc = make_sdesc(sKVa, C::kBoxBytes, 1024);
-    auto issue_s = [&](uint32_t slot) {
-        const uint64_t kb = k_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4));
+    auto issue_s = [&](uint32_t slot, int h) {
+        const uint64_t kb = k_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4) + (uint32_t)((h * kHalf * 128) >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-            if (leader) mma_ss(dS, q_desc + off, kb + off, idesc_s, kk > 0);
+            if (leader) mma_ss(dS + h * kHalf, q_desc + off, kb + off, idesc_s, kk > 0);
         }
-        if (leader) mma_commit(s_full);
+        if (leader) mma_commit(smem_u32(&sh->s_full[t][h]));
     };
     // O += P V: P from TMEM (8 columns = 16 keys per step), V MN-major in
     // shared memory (16 keys = two 8-row swizzle atoms = 2048 bytes per step;
     // the second 64-column chunk of V sits one box further on).  With a split
-    // P the low halves (64 columns further on) add a second product.
-    auto issue_pv = [&](uint32_t slot, bool first, bool split) {
+    // P the low halves (32 columns further on) add a second product.  Every
+    // P.V is committed to pv_done by step parity, for the rare O rescale.
+    auto issue_pv = [&](uint32_t slot, int h, bool zero, bool split) {
         const uint64_t vb = v_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-            const uint64_t b = vb + (uint64_t)(kk * (2048 >> 4));
-            if (leader) mma_ts(dO, dS + kk * 8, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < kHalf / 16; ++kk) {
+            const uint64_t b = vb + (uint64_t)((h * (kHalf / 16) + kk) * (2048 >> 4));
+            if (leader) mma_ts(dO, dS + h * kHalf + kk * 8, b, idesc_o, (zero && kk == 0) ? 0u : 1u);
         }
         if (split) {
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk) {
-                const uint64_t b = vb + (uint64_t)(kk * (2048 >> 4));
-                if (leader) mma_ts(dO, dS + 64 + kk * 8, b, idesc_o, 1u);
+            for (int kk = 0; kk < kHalf / 16; ++kk) {
+                const uint64_t b = vb + (uint64_t)((h * (kHalf / 16) + kk) * (2048 >> 4));
+                if (leader) mma_ts(dO, dS + h * kHalf + kHalf / 2 + kk * 8, b, idesc_o, 1u);
             }
         }
+        if (leader) mma_commit(smem_u32(&sh->pv_done[t][pv_it & 1]));
+        ++pv_it;
     };
     auto wait_kv = [&](uint32_t idx) {
         const bool r = W.wait_warp(smem_u32(&sh->kv_full[idx % C::kStages]), (idx / C::kStages) & 1);
@@ -299,11 +280,8 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         kv_it += 2 * (un.jhi - un.jlo);
         const int lo = t ? un.lo[1] : un.lo[0];
         const int hi = t ? un.hi[1] : un.hi[0];
-        const unsigned long long useq = (unsigned long long)q_it << 32;  // q_it counts units taken
-        const int hi0 = un.hi[0], lo0 = un.lo[0], hi1 = un.hi[1], lo1 = un.lo[1];
         auto kidx = [&](int j) { return kbase + 2 * (uint32_t)(j - un.jlo); };
         if (lo == hi) {
-            publish(useq | 0xFFFFFFFFull);
             if (leader) mbar_arrive(q_empty);
             for (int j = un.jlo; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
             continue;
@@ -311,38 +289,39 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         const bool split = kBf16 && tile_split_p(p.g, un.q0 + t * kTileM);
         for (int j = un.jlo; j < lo && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
         if (!ok || !(ok = wait_kv(kidx(lo)))) break;
-        issue_s(kidx(lo) % C::kStages);
+        issue_s(kidx(lo) % C::kStages, 0);
+        issue_s(kidx(lo) % C::kStages, 1);
         if (leader) mma_commit(smem_u32(&sh->kv_empty[kidx(lo) % C::kStages]));
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t v = kidx(j) + 1;
             if (j == hi - 1 && leader) mma_commit(q_empty);  // this tile's last S is issued
             // Every other condition of this step is met before P_j is waited
-            // for, so the MMAs go out as soon as P_j lands: V_j; K_(j+1) for the
-            // S issued right after P.V_j (its ring slot was freed by S(j-1) of
-            // both tiles, issued at least one step earlier, so it never waits on
-            // this step); the O accumulator at a unit's first step (freed by the
-            // previous epilogue, which precedes this unit's first P); and the
-            // other tile's turn (which never depends on this tile's P_j).
+            // for, so the MMAs go out as soon as each half of P_j lands: V_j;
+            // K_(j+1) for the S issued right after each P.V (its ring slot was
+            // freed by S(j-1) of both tiles, issued at least one step earlier,
+            // so it never waits on this step); and the O accumulator at a
+            // unit's first step (freed by the previous epilogue, which precedes
+            // this unit's first P).
             if (!(ok = wait_kv(v))) break;
             if (j + 1 < hi && !(ok = wait_kv(kidx(j + 1)))) break;
             const bool first = j == lo;
             if (first && o_cnt > 0 && !(ok = W.wait_warp(o_free, (o_cnt - 1) & 1))) break;
-            if (t == 1 && lo0 < hi0 && !(ok = wait_turn(useq | (unsigned long long)(j + 1 < hi0 ? j + 1 : hi0)))) break;
-            if (t == 0 && j - 1 >= lo1 && j - 1 < hi1 && !(ok = wait_turn(useq | (unsigned long long)j))) break;
-            if (!(ok = W.wait_warp(p_full, p_cnt & 1))) break;
-            ++p_cnt;
-            tc_fence_after();
-            issue_pv(v % C::kStages, first, split);
-            if (leader) mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
-            if (j == hi - 1) {
-                if (leader) mma_commit(o_done);
-                ++o_cnt;
-            } else {
-                const uint32_t k = kidx(j + 1);
-                issue_s(k % C::kStages);
-                if (leader) mma_commit(smem_u32(&sh->kv_empty[k % C::kStages]));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = W.wait_warp(smem_u32(&sh->p_full[t][h]), p_cnt[h] & 1))) break;
+                ++p_cnt[h];
+                tc_fence_after();
+                issue_pv(v % C::kStages, h, first && h == 0, split);
+                if (h == 1 && leader) mma_commit(smem_u32(&sh->kv_empty[v % C::kStages]));
+                if (j + 1 < hi) {
+                    const uint32_t k = kidx(j + 1) % C::kStages;
+                    issue_s(k, h);
+                    if (h == 1 && leader) mma_commit(smem_u32(&sh->kv_empty[k]));
+                } else if (h == 1) {
+                    if (leader) mma_commit(o_done);
+                    ++o_cnt;
+                }
             }
-            publish(useq | (unsigned long long)(j + 1));
         }
         for (int j = hi; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
     }
@@ -363,12 +342,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t ? C::kColS1 : C::kColS0);
     const uint32_t tO = tmem + lane_base + (t ? C::kColO1 : C::kColO0);
-    const uint32_t s_full = smem_u32(&sh->s_full[t]);
-    const uint32_t p_full = smem_u32(&sh->p_full[t]);
     const uint32_t o_done = smem_u32(&sh->o_done[t]);
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
     const float c2 = p.scale_log2;
-    uint32_t s_cnt = 0, u_cnt = 0, q_cnt = 0;
+    uint32_t s_cnt[2] = {0, 0};
+    uint32_t u_cnt = 0, q_cnt = 0, g = 0;  // g: S halves taken so far (P.V steps)
     bool ok = true;
     for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
@@ -385,7 +363,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             if (jlo_t < jhi_t && qi < p.g.N) {
                 const long long pos = (long long)p.rope_pos0 + qi;
                 rope_q_row<D, kBf16, C::kBoxBytes>(sQ + t * C::kTileBytes, row, p.rope_cos + pos * (D / 2),
-                                     p.rope_sin + pos * (D / 2), p.rope_style);
+                                                   p.rope_sin + pos * (D / 2), p.rope_style);
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&sh->q_ready[t]));
@@ -394,14 +372,24 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
         const bool split = kBf16 && tile_split_p(p.g, r0);
         float m_ref = -INFINITY;
         float l = 0.f;
-        for (int j = jlo_t; j < jhi_t; ++j) {
-            if (!(ok = W.wait_warp(s_full, s_cnt & 1))) break;
-            ++s_cnt;
-            tc_fence_after();
-            float lsum;
-            softmax_tile<D, kBf16, kPosScale>(p.g, tS, tO, c2, r0, qi, j, j == jlo_t, split, m_ref, l, lsum);
-            mbar_arrive(p_full);
-            l += lsum;
+        for (int j = jlo_t; j < jhi_t && ok; ++j) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = W.wait_warp(smem_u32(&sh->s_full[t][h]), s_cnt[h] & 1))) break;
+                ++s_cnt[h];
+                tc_fence_after();
+                // The P.V of the previous half is the only product that can
+                // still be adding into O here.
+                const uint32_t gp = g - 1;
+                auto wait_pv = [&]() { return W.wait_warp(smem_u32(&sh->pv_done[t][gp & 1]), (gp >> 1) & 1); };
+                float lsum;
+                if (!(ok = softmax_half<D, kBf16, kPosScale>(p.g, tS + h * (kTileN / 2), tO, c2, r0, qi, j, h,
+                                                             j == jlo_t && h == 0, split, m_ref, l, lsum, wait_pv)))
+                    break;
+                mbar_arrive(smem_u32(&sh->p_full[t][h]));
+                l += lsum;
+                ++g;
+            }
         }
         if (!ok) break;
 
@@ -466,13 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
             mbar_init(smem_u32(&sh->kv_empty[s]), 2);
         }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(smem_u32(&sh->s_full[t]), 1);
-            mbar_init(smem_u32(&sh->p_full[t]), 128);
+            for (int h = 0; h < 2; ++h) {
+                mbar_init(smem_u32(&sh->s_full[t][h]), 1);
+                mbar_init(smem_u32(&sh->p_full[t][h]), 128);
+                mbar_init(smem_u32(&sh->pv_done[t][h]), 1);
+            }
             mbar_init(smem_u32(&sh->o_done[t]), 1);
             mbar_init(smem_u32(&sh->o_free[t]), 128);
         }
-        sh->progress[0] = 0ull;
-        sh->progress[1] = 0ull;
         mbar_init(smem_u32(&sh->drain[0]), 1);
         mbar_init(smem_u32(&sh->drain[1]), 1);
         sh->abort = 0;

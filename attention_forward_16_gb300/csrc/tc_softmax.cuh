@@ -1,8 +1,9 @@
-// The per-tile softmax step and the in-place rotation of a Q tile, shared by
-// the fused forward kernels (one-CTA fa_tc.cu and CTA-pair fa_tc2.cu).
+// The softmax step of the one-CTA forward kernel (fa_tc.cu) and the in-place
+// rotation of a Q tile shared by both fused forward kernels (fa_tc.cu and the
+// CTA-pair fa_tc2.cu).
 //
-// One thread owns one query row of a 128-row tile whose scores S (fp32, 128
-// columns) sit in tensor memory.  The step follows the online softmax of
+// One thread owns one query row of a 128-row tile whose scores S (fp32) sit
+// in tensor memory, 64 keys at a time.  The step follows the online softmax of
 // "Ascend C advanced practice: high-performance FlashAttention-2-style
 // tile-level fused attention" (section 1.2) and the ops-transformer
 // walk-through ("online softmax: incremental update"): mask, running row
@@ -25,24 +26,39 @@ namespace fa {
 constexpr float kTau = 8.0f;                      // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// One key tile j of one row (query qi, tile start r0).  tS / tO: this warp's
-// lane base plus the tile's S / O columns.  c2 = scale * log2(e).  On return
-// P is in tensor memory (columns [0, 64) as 16-bit pairs; with `split` the
-// bf16 low parts in [64, 128)), every tensor-memory store has completed and
-// been fenced for a following thread synchronisation, m_ref / l are updated
-// (l rescaled, not yet increased) and `lsum` holds this tile's row sum.
-template <int D, bool kBf16, bool kPosScale>
-__device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_t tO, float c2, int r0, int qi, int j,
-                                             bool first, bool split, float& m_ref, float& l, float& lsum) {
+// Bit i (0 <= i < 32) set iff lo <= i <= hi: the visible columns of one
+// 32-column chunk, from the row's visible interval taken relative to the
+// chunk's first column.
+__device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
+    const uint32_t upto = hi >= 31 ? 0xffffffffu : hi < 0 ? 0u : (2u << hi) - 1u;
+    const uint32_t from = lo <= 0 ? 0xffffffffu : lo > 31 ? 0u : 0xffffffffu << lo;
+    return upto & from;
+}
+
+// One half (64 keys) of key tile j for one row (query qi, tile start r0):
+// an online-softmax step of its own.  tS / tO: this warp's lane base plus the
+// half's 64 S columns / the tile's O columns.  c2 = scale * log2(e).  On
+// return P is in tensor memory over the half's first 32 columns (16-bit
+// pairs; with `split` the bf16 low parts in the next 32), every tensor-memory
+// store has completed and been fenced for a following thread
+// synchronisation, m_ref / l are updated (l rescaled, not yet increased) and
+// `lsum` holds this half's row sum.  When the running max moves by more than
+// kTau, O is rescaled in place after `wait_pv()` has confirmed that the
+// product still adding into O (the previous half's P.V) has completed; false
+// if that wait gave up.
+template <int D, bool kBf16, bool kPosScale, class WaitPv>
+__device__ __forceinline__ bool softmax_half(const Geom& g, uint32_t tS, uint32_t tO, float c2, int r0, int qi, int j,
+                                             int h, bool first, bool split, float& m_ref, float& l, float& lsum,
+                                             const WaitPv& wait_pv) {
     using namespace ptx;
-    uint32_t s[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+    uint32_t s[2][32];
+    tmem_ld32(tS, s[0]);
+    tmem_ld32(tS + 32, s[1]);
     tmem_wait_ld();
 
     if (!kPosScale) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 float a, b;
@@ -51,23 +67,27 @@ __device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_
                 s[c][i + 1] = f2u(b);
             }
     }
-    if (tile_needs_mask(g, r0, j)) {
+    if (tile_needs_mask(g, r0, j)) {  // the same for the whole tile
+        // The row's visible interval as a bit set per 32-column chunk; a chunk
+        // the whole warp sees in full is skipped.
         int c_lo, c_hi;
         row_visible_cols(g, qi, j, c_lo, c_hi);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c) {
+            const int c0 = 32 * (2 * h + c);
+            const uint32_t vis = span_bits(c_lo - c0, c_hi - c0);
+            if (__all_sync(0xffffffffu, vis == 0xffffffffu)) continue;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int col = c * 32 + i;
-                if (col < c_lo || col > c_hi) s[c][i] = f2u(-INFINITY);
-            }
+            for (int i = 0; i < 32; ++i)
+                if (!((vis >> i) & 1u)) s[c][i] = f2u(-INFINITY);
+        }
     }
-    // Row max: 64 three-input maxes spread over 8 independent chains.
+    // Row max: 32 three-input maxes spread over 8 independent chains.
     float mxk[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mxk[k] = fmaxf(u2f(s[0][2 * k]), u2f(s[0][2 * k + 1]));
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int i = (c == 0 ? 16 : 0); i < 32; i += 2) {
             const int k = (i >> 1) & 7;
@@ -93,7 +113,7 @@ __device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_
         // 16-bit pairs; the row sum runs over four packed accumulators.
         float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -113,9 +133,9 @@ __device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_
         l0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
         l1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
     } else {
-        // p = hi + lo, both bf16: hi in columns [0, 64), lo in [64, 128).
+        // p = hi + lo, both bf16: hi in columns [0, 32), lo in [32, 64).
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -128,27 +148,33 @@ __device__ __forceinline__ void softmax_tile(const Geom& g, uint32_t tS, uint32_
                 l0 += a;
                 l1 += b;
             }
-            tmem_st16(tS + c * 16, hw);
-            tmem_st16(tS + 64 + c * 16, lw);
+            tmem_st16(tS + 16 * c, hw);
+            tmem_st16(tS + 32 + 16 * c, lw);
         }
     }
+    bool ok = true;
     if (!first && __any_sync(0xffffffffu, resc)) {
-        // Rare: the running max moved by more than kTau; rescale this row of O.
-        // O is stable here: the MMA that wrote it completed before S_j did, and
-        // the next P.V waits for this warpgroup's arrival below.
+        // Rare: the running max moved by more than kTau; rescale this row of O
+        // once the P.V still in flight has landed (the next one waits for this
+        // warpgroup's arrival).
+        ok = wait_pv();
+        if (ok) {
+            tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
+                for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                tmem_st32(tO + c * 32, o);
+            }
         }
     }
     tmem_wait_st();
     tc_fence_before();
     lsum = l0 + l1;
+    return ok;
 }
 
 // ------------------------------------------- rotary embedding of a Q tile
