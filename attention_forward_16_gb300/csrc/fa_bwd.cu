@@ -77,7 +77,10 @@ struct __align__(16) BwdCtl {
     uint64_t fixed_full;
     uint64_t qd_full;  // dq: Q and dO rows stored in TMEM (one arrival per elementwise thread)
     uint64_t ring_full[4], ring_empty[4];
-    uint64_t s_full, s_free, dp_full, p_full, ds_full, acc_done, drain;
+    // Per column part of a tile in the dQ kernel (its 64 keys of S and dP),
+    // whose parts run on their own barriers; the dK/dV kernel uses index 0.
+    uint64_t s_full[kParts], s_free[kParts], dp_full[kParts], p_full[kParts], ds_full[kParts];
+    uint64_t acc_done, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -112,6 +115,7 @@ template <int D, bool kBf16>
 struct Mma {
     static constexpr uint32_t kIdescRows = make_idesc(kBf16, kTileM, kTileN, false);  // 128 x 128, K = D
     static constexpr uint32_t kIdescCols = make_idesc(kBf16, kTileM, D, true);         // 128 x D, K = 128
+    static constexpr uint32_t kIdescPart = make_idesc(kBf16, kTileM, kColsPerPart, false);  // 128 x 64, K = D
     // dst[128 x 128] = A[128 x D] B[128 x D]^T, both from shared memory.
     // Called by the whole issuing warp; `leader` (one elected lane) issues.
     // Descriptors advance by encoded offsets (address / 16 in the low field;
@@ -122,6 +126,30 @@ struct Mma {
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk / 4) * BwdCfg<D>::kBoxBytes + (kk % 4) * 32) >> 4;
             if (leader) mma_ss(dst, ad + off, bd + off, kIdescRows, kk > 0);
+        }
+    }
+    // Part h of dst[128 x 128] = A[128 x D] B[128 x D]^T with A in TMEM as
+    // 16-bit pairs (a TS product: only B is read from shared memory): its 64
+    // columns dst[:, 64h, 64h + 64) from rows [64h, 64h + 64) of B, which
+    // start 8 swizzle atoms into each column chunk.
+    static __device__ __forceinline__ void rows_part_t(uint32_t dst, uint32_t ta, uint32_t b, int h, bool leader) {
+        const uint64_t bd = make_sdesc(b, 16, 1024) + (uint64_t)((h * kColsPerPart * 128) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk / 4) * BwdCfg<D>::kBoxBytes + (kk % 4) * 32) >> 4;
+            if (leader) mma_ts(dst + h * kColsPerPart, ta + kk * 8, bd + off, kIdescPart, kk > 0);
+        }
+    }
+    // dst[128 x D] (+)= T_h[128 x 64] B_h[64 x D]: part h of cols() below.
+    static __device__ __forceinline__ void cols_part(uint32_t dst, uint32_t t, uint32_t b, int h, bool acc,
+                                                     bool leader) {
+        constexpr int kSteps = kColsPerPart / 16;
+        const uint64_t bd = make_sdesc(b, BwdCfg<D>::kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk) {
+            if (leader)
+                mma_ts(dst, t + h * kColsPerPart + kk * 8, bd + (uint64_t)((h * kSteps + kk) * (2048 >> 4)),
+                       kIdescCols, (acc || kk > 0) ? 1u : 0u);
         }
     }
     // dst[128 x D] (+)= T[128 x 128] B[128 x D]: T 16-bit in TMEM, its K
@@ -139,18 +167,22 @@ struct Mma {
     }
 };
 
-__device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count) {
+// `ew_count`: arrivals that complete an elementwise barrier (every
+// elementwise thread, or one part's threads where the parts run apart).
+__device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count, int ew_count) {
     mbar_init(smem_u32(&sh->fixed_full), 1);
     mbar_init(smem_u32(&sh->qd_full), kEwThreads);
     for (int s = 0; s < 4; ++s) {
         mbar_init(smem_u32(&sh->ring_full[s]), 1);
         mbar_init(smem_u32(&sh->ring_empty[s]), ring_empty_count);
     }
-    mbar_init(smem_u32(&sh->s_full), 1);
-    mbar_init(smem_u32(&sh->s_free), kEwThreads);
-    mbar_init(smem_u32(&sh->dp_full), 1);
-    mbar_init(smem_u32(&sh->p_full), kEwThreads);
-    mbar_init(smem_u32(&sh->ds_full), kEwThreads);
+    for (int h = 0; h < kParts; ++h) {
+        mbar_init(smem_u32(&sh->s_full[h]), 1);
+        mbar_init(smem_u32(&sh->s_free[h]), ew_count);
+        mbar_init(smem_u32(&sh->dp_full[h]), 1);
+        mbar_init(smem_u32(&sh->p_full[h]), ew_count);
+        mbar_init(smem_u32(&sh->ds_full[h]), ew_count);
+    }
     mbar_init(smem_u32(&sh->acc_done), 1);
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
@@ -235,7 +267,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     const int ni = ihi - ilo;
     const int n_items = ni * p.G;  // (query head of the group, query tile) pairs, head-major
 
-    if (threadIdx.x == 0) init_ctl(sh, 1);
+    if (threadIdx.x == 0) init_ctl(sh, 1, kEwThreads);
     if (warp == kWarpMmaB) {
         tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
         tmem_relinquish();
@@ -292,27 +324,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
         if (ok) {
             tc_fence_after();
             M::rows(tS, sK, stage(0), leader);                       // S^T = K Q^T
-            if (leader) mma_commit(smem_u32(&sh->s_full));
+            if (leader) mma_commit(smem_u32(&sh->s_full[0]));
             M::rows(tDP, sV, stage(0) + C::kTileBytes, leader);      // dP^T = V dO^T
-            if (leader) mma_commit(smem_u32(&sh->dp_full));
+            if (leader) mma_commit(smem_u32(&sh->dp_full[0]));
         }
         for (int n = 0; n < n_items && ok; ++n) {
-            if (!(ok = W.wait_warp(smem_u32(&sh->p_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->p_full[0]), n & 1))) break;
             tc_fence_after();
             M::cols(tDV, tS, stage(n) + C::kTileBytes, n > 0, leader);   // dV += P^T dO
             if (n + 1 < n_items) {
                 if (!(ok = ring_full(n + 1))) break;
                 tc_fence_after();
                 M::rows(tS, sK, stage(n + 1), leader);
-                if (leader) mma_commit(smem_u32(&sh->s_full));
+                if (leader) mma_commit(smem_u32(&sh->s_full[0]));
             }
-            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full[0]), n & 1))) break;
             tc_fence_after();
             M::cols(tDK, tDP, stage(n), n > 0, leader);                  // dK += dS^T Q
             if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
             if (n + 1 < n_items) {
                 M::rows(tDP, sV, stage(n + 1) + C::kTileBytes, leader);
-                if (leader) mma_commit(smem_u32(&sh->dp_full));
+                if (leader) mma_commit(smem_u32(&sh->dp_full[0]));
             }
         }
         if (leader) mma_commit(smem_u32(&sh->acc_done));
@@ -337,7 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             const float4* dsum =
                 reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * (kColsPerPart / 4);
             if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1))) break;
-            if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->s_full[0]), n & 1))) break;
             tc_fence_after();
             uint32_t s[kChunks][32];
             ld_part(tS, s);
@@ -376,9 +408,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&sh->p_full));
+            mbar_arrive(smem_u32(&sh->p_full[0]));
             // dS^T: p * (dP - Dsum_q), written over dP columns of this half already read
-            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full[0]), n & 1))) break;
             tc_fence_after();
             uint32_t d[kChunks][32];
             ld_part(tDP, d);
@@ -400,7 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&sh->ds_full));
+            mbar_arrive(smem_u32(&sh->ds_full[0]));
         }
         // epilogue: this part's columns of dV and scale * dK for the keys that exist
         const bool live = kc < p.g.N;
@@ -446,7 +478,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
     if (r0 < p.g.N) kv_tile_range(p.g, r0, r0 + kTileM < p.g.N ? r0 + kTileM : p.g.N, jlo, jhi);
     const int n_items = jhi - jlo;
 
-    if (threadIdx.x == 0) init_ctl(sh, 1);
+    if (threadIdx.x == 0) init_ctl(sh, 1, kEwThreads / kParts);
     if (warp == kWarpMmaB) {
         tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
         tmem_relinquish();
@@ -485,38 +517,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStagesQ]), (n / C::kStagesQ) & 1);
         };
         // S = Q K^T and dP = dO V^T with the stationary A operand read from TMEM
-        // (TS products): only K and V come from shared memory.
-        auto rows_t = [&](uint32_t dst, uint32_t ta, uint32_t b) {
-            const uint64_t bd = make_sdesc(b, 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-                if (leader) mma_ts(dst, ta + kk * 8, bd + off, M::kIdescRows, kk > 0);
-            }
-        };
+        // (TS products): only K and V come from shared memory, so products of
+        // 64 keys keep the tensor core at full rate.  Each column part h (64
+        // keys) has its own barriers: part h's next S goes out once its S has
+        // been read into registers, its next dP once the dQ product has read
+        // its dS, while the other part's elementwise work still runs.
         bool ok = W.wait_warp(smem_u32(&sh->qd_full), 0) && ring_full(0);
         if (ok) {
             tc_fence_after();
-            rows_t(tS, tQ, stage(0));                                // S = Q K^T
-            if (leader) mma_commit(smem_u32(&sh->s_full));
-            rows_t(tDP, tDO, stage(0) + C::kTileBytes);              // dP = dO V^T
-            if (leader) mma_commit(smem_u32(&sh->dp_full));
+#pragma unroll
+            for (int h = 0; h < kParts; ++h) {
+                M::rows_part_t(tS, tQ, stage(0), h, leader);                    // S = Q K^T
+                if (leader) mma_commit(smem_u32(&sh->s_full[h]));
+            }
+#pragma unroll
+            for (int h = 0; h < kParts; ++h) {
+                M::rows_part_t(tDP, tDO, stage(0) + C::kTileBytes, h, leader);  // dP = dO V^T
+                if (leader) mma_commit(smem_u32(&sh->dp_full[h]));
+            }
         }
         for (int n = 0; n < n_items && ok; ++n) {
-            if (n + 1 < n_items) {
-                // the next S may overwrite S once its row loads are done
-                if (!(ok = W.wait_warp(smem_u32(&sh->s_free), n & 1) && ring_full(n + 1))) break;
-                tc_fence_after();
-                rows_t(tS, tQ, stage(n + 1));
-                if (leader) mma_commit(smem_u32(&sh->s_full));
+            const bool more = n + 1 < n_items;
+            if (more) {
+                if (!(ok = ring_full(n + 1))) break;
+#pragma unroll
+                for (int h = 0; h < kParts; ++h) {
+                    // the next S may overwrite S once its row loads are done
+                    if (!(ok = W.wait_warp(smem_u32(&sh->s_free[h]), n & 1))) break;
+                    tc_fence_after();
+                    M::rows_part_t(tS, tQ, stage(n + 1), h, leader);
+                    if (leader) mma_commit(smem_u32(&sh->s_full[h]));
+                }
+                if (!ok) break;
             }
-            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full), n & 1))) break;
-            tc_fence_after();
-            M::cols(tDQ, tDP, stage(n), n > 0, leader);               // dQ += dS K
-            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStagesQ]));
-            if (n + 1 < n_items) {
-                rows_t(tDP, tDO, stage(n + 1) + C::kTileBytes);
-                if (leader) mma_commit(smem_u32(&sh->dp_full));
+#pragma unroll
+            for (int h = 0; h < kParts; ++h) {
+                if (!(ok = W.wait_warp(smem_u32(&sh->ds_full[h]), n & 1))) break;
+                tc_fence_after();
+                M::cols_part(tDQ, tDP, stage(n), h, n > 0 || h > 0, leader);     // dQ += dS K
+                if (h == kParts - 1 && leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStagesQ]));
+                if (more) {
+                    M::rows_part_t(tDP, tDO, stage(n + 1) + C::kTileBytes, h, leader);
+                    if (leader) mma_commit(smem_u32(&sh->dp_full[h]));
+                }
             }
         }
         if (leader) mma_commit(smem_u32(&sh->acc_done));
@@ -569,12 +612,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
         }
         for (int n = 0; n < n_items && ok; ++n) {
             const int j = jlo + n;
-            if (!(ok = W.wait_warp(smem_u32(&sh->s_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->s_full[hf]), n & 1))) break;
             tc_fence_after();
             uint32_t s[kChunks][32];
             ld_part(tS, s);
             tc_fence_before();
-            mbar_arrive(smem_u32(&sh->s_free));
+            mbar_arrive(smem_u32(&sh->s_free[hf]));
             const bool masked = tile_needs_mask(p.g, r0, j);  // uniform over the CTA
             int c_lo = 0, c_hi = kTileN - 1;
             if (masked) row_visible_cols(p.g, qi, j, c_lo, c_hi);
@@ -594,7 +637,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
                     s[cc][v] = f2u(e0);
                     s[cc][v + 1] = f2u(e1);
                 }
-            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full), n & 1))) break;
+            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full[hf]), n & 1))) break;
             tc_fence_after();
             uint32_t d[kChunks][32];
             ld_part(tDP, d);
@@ -612,7 +655,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&sh->ds_full));
+            mbar_arrive(smem_u32(&sh->ds_full[hf]));
         }
         const bool live = qi < p.g.N;
         const size_t orow = (size_t)row_index(p.layout, b, h, live ? qi : 0, p.H, p.g.N);
