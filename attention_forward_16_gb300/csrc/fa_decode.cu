@@ -505,6 +505,313 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
     }
 }
 
+// ------------------------------------------------- tensor-core decode rows
+// Two to sixteen query rows per (batch, K/V head), 16-bit inputs: the scores
+// and P.V of a block of 16 keys are warp-level m16n8k16 MMAs (rows padded to
+// 16), so the per-key work no longer costs an FMA and a shuffle per element
+// on the CUDA cores, and the kernel is left with the streaming of K and V.
+// The scores' accumulator fragments are, element for element, the A operand
+// fragments of the P.V product, so P never leaves registers; it enters that
+// product as hi + lo, two 16-bit parts, which keeps the result as close to
+// the fp32 arithmetic of the other decode kernels as their own rounding (the
+// tensor cores have room to spare: the kernel is bound by HBM).
+//
+// Each warp streams its own 16-key blocks (round robin over the split)
+// through a two-stage shared-memory ring filled by 16-byte asynchronous
+// copies: the next block lands while this one is computed.  At 64 KB a CTA,
+// three CTAs (twelve warps) share an SM, which hides the MMA and shuffle
+// latencies that a deeper ring with four or eight warps an SM left exposed.
+// Rows are 16-byte-chunk swizzled (chunk c of row r at c ^ (r % 8)), so the
+// ldmatrix reads are free of bank conflicts.
+namespace mmadec {
+
+constexpr int kKeys = 16;   // keys per block
+constexpr int kStages = 2;  // ring depth per warp (three CTAs per SM fit)
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// c[16 x 8] += a[16 x 16] b[16 x 8], fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <typename T>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) return ptx::pack_bf16x2(lo, hi);
+    else return ptx::pack_f16x2(lo, hi);
+}
+// The two 16-bit values of a packed word, as fp32.
+template <typename T>
+__device__ __forceinline__ float2 unpack16(uint32_t w) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    else return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+// p as an unevaluated sum hi + lo of two 16-bit values (lo = the rounding
+// error of hi), so that P.V keeps about twice the 16-bit precision of p.
+template <typename T>
+__device__ __forceinline__ void split16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+    hi = pack16<T>(p0, p1);
+    const float2 h = unpack16<T>(hi);
+    lo = pack16<T>(p0 - h.x, p1 - h.y);
+}
+
+template <int D>
+struct Cfg {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kChunks = kRowBytes / 16;         // 16-byte chunks per row
+    static constexpr int kBlockBytes = kKeys * kRowBytes;  // one block of K (or V)
+    static constexpr int kStageBytes = 2 * kBlockBytes;    // K | V
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kRingBytes = kDecWarps * kWarpBytes;
+    static constexpr int kMergeBytes = kDecWarps * kDecodeMaxQ * (D + 2) * 4;
+    static constexpr int kSmem = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+    static __device__ __forceinline__ uint32_t swz(int row, int chunk) {
+        return (uint32_t)(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
+    }
+};
+
+}  // namespace mmadec
+
+// One CTA = one (b, K/V head, split); 16-bit K/V, 2 <= G * Nq <= 16.
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads) fa_decode_mma_kernel(const DecodeParams p) {
+    using namespace mmadec;
+    using C = Cfg<D>;
+    constexpr float kTauDec = 8.0f;  // lazy rescale threshold (log2 units), as in the forward
+    extern __shared__ __align__(128) uint8_t dec_smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;  // fragment row (and row + 8)
+    const int q4 = lane & 3;  // fragment column pair
+    const int split = blockIdx.x % p.n_splits;
+    const long long bh = blockIdx.x / p.n_splits;
+    const int len = dec_len(p, bh);
+    const int k0 = split * p.chunk;
+    const int k1 = min(len, k0 + p.chunk);
+    const int rows = p.G * p.Nq;
+    const T* qg = static_cast<const T*>(p.q);
+    const T* kg = static_cast<const T*>(p.k);
+    const T* vg = static_cast<const T*>(p.v);
+    const uint32_t ring = ptx::smem_u32(dec_smem) + warp * C::kWarpBytes;
+
+    // Q as the A operand of every score product: rows g and g + 8 (zero past
+    // `rows`), columns 16 ks + 2 q4 (+1) and 16 ks + 8 + 2 q4 (+1).
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = g + 8 * hr;
+        const uint32_t* qrow = r < rows ? reinterpret_cast<const uint32_t*>(qg + dec_qrow(p, bh, r, D)) : nullptr;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qa[ks][hr] = qrow ? qrow[(16 * ks + 2 * q4) / 2] : 0u;
+            qa[ks][2 + hr] = qrow ? qrow[(16 * ks + 8 + 2 * q4) / 2] : 0u;
+        }
+    }
+
+    // Blocks of this split for this warp: b = warp, warp + 4, ...
+    const int nb = k1 > k0 ? (k1 - k0 + kKeys - 1) / kKeys : 0;
+    auto load_block = [&](int b, int st) {
+        const uint32_t sK = ring + st * C::kStageBytes, sV = sK + C::kBlockBytes;
+        const int base = k0 + b * kKeys;
+        // lane covers chunk (lane % kChunks) of rows lane / kChunks + (32 / kChunks) i
+        constexpr int kRowsPerPass = 32 / C::kChunks;
+        const int ch = lane % C::kChunks;
+        // A whole block inside one page (or an unpaged cache) is 16 rows at a
+        // fixed stride: one address computation (one page lookup) per block.
+        const bool even = base + kKeys <= k1 &&
+                          (!p.block_table || (base >> p.page_shift) == ((base + kKeys - 1) >> p.page_shift));
+        const size_t row0 = even ? dec_krow(p, bh, base, D) : 0;
+        const size_t stride = (p.block_table || p.layout != LAYOUT_BHND) ? (size_t)p.Hkv * D : (size_t)D;
+#pragma unroll
+        for (int i = 0; i < kKeys / kRowsPerPass; ++i) {
+            const int row = lane / C::kChunks + kRowsPerPass * i;
+            int j = base + row;
+            if (j >= k1) j = k1 - 1;  // clamp: tail keys are masked below
+            const size_t off = (even ? row0 + (size_t)row * stride : dec_krow(p, bh, j, D)) + ch * 8;
+            cp_async16(sK + C::swz(row, ch), kg + off);
+            cp_async16(sV + C::swz(row, ch), vg + off);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (warp + kDecWarps * s < nb) load_block(warp + kDecWarps * s, s);
+        cp_async_commit();
+    }
+
+    // Keys every query sees (see the lane-group kernel above).
+    const long long vis_lo = p.win_l >= 0 ? (long long)len - 1 - p.win_l : LLONG_MIN;
+    const long long vis_hi = p.win_r >= 0 ? (long long)len - p.Nq + p.win_r : LLONG_MAX;
+
+    float o[D / 8][4];
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    // ldmatrix row addresses: key rows (lane & 7) + 8 (lane >> 4) at chunk
+    // offset (lane >> 3) & 1 for K; key rows (lane & 7) + 8 ((lane >> 3) & 1)
+    // at chunk offset lane >> 4 for V (transposed).
+    const int krow = (lane & 7) + ((lane >> 4) << 3), kch = (lane >> 3) & 1;
+    const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3), vch = lane >> 4;
+
+    for (int it = 0;; ++it) {
+        const int b = warp + kDecWarps * it;
+        if (b >= nb) break;
+        const int nxt = b + kDecWarps * (kStages - 1);
+        if (nxt < nb) load_block(nxt, (it + kStages - 1) % kStages);
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        const uint32_t sK = ring + (it % kStages) * C::kStageBytes, sV = sK + C::kBlockBytes;
+        const int base = k0 + b * kKeys;
+
+        // S = Q K^T for 16 rows x 16 keys (two 8-key halves), in log2 units.
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t kb[4];
+            ldsm_x4(kb, sK + C::swz(krow, 2 * ks + kch));
+            mma16816<T>(s[0], qa[ks], kb[0], kb[1]);
+            mma16816<T>(s[1], qa[ks], kb[2], kb[3]);
+        }
+        const bool full_block = base >= vis_lo && (long long)base + kKeys - 1 <= vis_hi && base + kKeys <= k1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                s[h][e] *= p.scale_log2;
+                if (!full_block) {
+                    const int j = base + 8 * h + 2 * q4 + (e & 1);
+                    const int r = g + 8 * (e >> 1);
+                    if (j >= k1 || !dec_visible(p, r % p.Nq, j, len)) s[h][e] = -INFINITY;
+                }
+            }
+
+        // Online softmax per row (g: elements 0, 1; g + 8: elements 2, 3); the
+        // four lanes of a quad hold one row's 16 scores.  The reference max
+        // moves lazily, only when the block's max passes it by kTauDec.
+        uint32_t pa[4], pl[4];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            float mx = fmaxf(fmaxf(s[0][2 * hr], s[0][2 * hr + 1]), fmaxf(s[1][2 * hr], s[1][2 * hr + 1]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            if (mx > m[hr] + kTauDec) {  // also the first finite max (m = -inf)
+                const float a = m[hr] == -INFINITY ? 0.f : ptx::ex2(m[hr] - mx);
+                l[hr] *= a;
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o[nd][2 * hr] *= a;
+                    o[nd][2 * hr + 1] *= a;
+                }
+                m[hr] = mx;
+            }
+            const float neg = m[hr] == -INFINITY ? 0.f : -m[hr];
+            const float p0 = ptx::ex2(s[0][2 * hr] + neg), p1 = ptx::ex2(s[0][2 * hr + 1] + neg);
+            const float p2 = ptx::ex2(s[1][2 * hr] + neg), p3 = ptx::ex2(s[1][2 * hr + 1] + neg);
+            l[hr] += (p0 + p1) + (p2 + p3);
+            split16<T>(p0, p1, pa[hr], pl[hr]);          // keys 2 q4, +1 of the first 8
+            split16<T>(p2, p3, pa[2 + hr], pl[2 + hr]);  // the same of the second 8
+        }
+
+        // O += P V: V rows are the K dimension (transposed ldmatrix), two
+        // 8-column tiles of O per load.
+#pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+            uint32_t vb[4];
+            ldsm_x4_t(vb, sV + C::swz(vrow, nd + vch));
+            mma16816<T>(o[nd], pa, vb[0], vb[1]);
+            mma16816<T>(o[nd + 1], pa, vb[2], vb[3]);
+            mma16816<T>(o[nd], pl, vb[0], vb[1]);
+            mma16816<T>(o[nd + 1], pl, vb[2], vb[3]);
+        }
+        __syncwarp();  // this stage is refilled by a later iteration's copies
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring; it becomes the merge area
+
+    // Per-warp state: the quad sums l; rows g and g + 8 of O.
+    float* st = reinterpret_cast<float*>(dec_smem) + (size_t)warp * kDecodeMaxQ * (D + 2);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        float lv = l[hr];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 1);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 2);
+        const int r = g + 8 * hr;
+        if (r < rows) {
+            float* row = st + r * (D + 2);
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) {
+                row[8 * nd + 2 * q4] = o[nd][2 * hr];
+                row[8 * nd + 2 * q4 + 1] = o[nd][2 * hr + 1];
+            }
+            if (q4 == 0) {
+                row[D] = m[hr];
+                row[D + 1] = lv;
+            }
+        }
+    }
+    __syncthreads();
+    constexpr int DV = D / 32;
+    const float* dsm = reinterpret_cast<const float*>(dec_smem);
+    for (int i = warp; i < rows; i += kDecWarps) {
+        float M = -INFINITY;
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, dsm[((size_t)w * kDecodeMaxQ + i) * (D + 2) + D]);
+        float Lsum = 0.f, ov[DV];
+#pragma unroll
+        for (int e = 0; e < DV; ++e) ov[e] = 0.f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kDecWarps; ++w) {
+                const float* sw = dsm + ((size_t)w * kDecodeMaxQ + i) * (D + 2);
+                const float a = sw[D] == -INFINITY ? 0.f : ptx::ex2(sw[D] - M);
+                Lsum += a * sw[D + 1];
+#pragma unroll
+                for (int e = 0; e < DV; ++e) ov[e] = fmaf(a, sw[lane * DV + e], ov[e]);
+            }
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kDecLn2 : -INFINITY;
+        if (p.n_splits == 1) {
+            T* ob = static_cast<T*>(p.o) + dec_qrow(p, bh, i, D) + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) ob[e] = from_float<T>(ov[e] * inv);
+            if (p.lse && lane == 0) p.lse[(size_t)bh * rows + i] = lse;
+        } else {
+            const size_t prow = ((size_t)bh * p.n_splits + split) * rows + i;
+            float* po = p.part_o + prow * D + lane * DV;
+#pragma unroll
+            for (int e = 0; e < DV; ++e) po[e] = ov[e] * inv;
+            if (lane == 0) p.part_lse[prow] = lse;
+        }
+    }
+}
+
+
 // One warp per output row: O = sum_s e^{LSE_s - LSE} O_s.
 template <typename T, int DV>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
@@ -567,14 +874,30 @@ cudaError_t launch_rows(const DecodeParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Query count buckets keep the per-row register arrays no larger than needed;
-// two to four rows take the lane-group kernel.
+template <typename T, int D>
+cudaError_t launch_mma(const DecodeParams& p, cudaStream_t s) {
+    const long long blocks = (long long)p.BH * p.n_splits;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    constexpr int smem = mmadec::Cfg<D>::kSmem;
+    auto kern = fa_decode_mma_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)blocks, kDecThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// One query row: the one-key-per-warp kernel.  Two or more rows: with 16-bit
+// inputs the tensor-core kernel; fp32 keeps the CUDA-core kernels (the lane-
+// group one for up to four rows), whose per-row register arrays are sized by
+// these buckets.
 template <typename T, int DV>
 cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
     const int rows = p.G * p.Nq;
-    cudaError_t e = rows == 1   ? launch_split<T, DV, 1>(p, s)
-                    : rows <= 4 ? launch_rows<T, 32 * DV>(p, s)
-                                : launch_split<T, DV, kDecodeMaxQ>(p, s);
+    constexpr bool k16 = !std::is_same<T, float>::value;
+    cudaError_t e = rows == 1         ? launch_split<T, DV, 1>(p, s)
+                    : k16             ? launch_mma<T, 32 * DV>(p, s)
+                    : rows <= 4       ? launch_rows<T, 32 * DV>(p, s)
+                                      : launch_split<T, DV, kDecodeMaxQ>(p, s);
     if (e != cudaSuccess || p.n_splits == 1) return e;
     const long long all_rows = (long long)p.BH * rows;
     fa_decode_combine_kernel<T, DV><<<(unsigned)((all_rows + 3) / 4), 128, 0, s>>>(p);
@@ -598,7 +921,7 @@ int decode_ctas_per_sm(int rows, int D) {
     static std::atomic<int> cache[kMaxDev][3][2];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    const int cls = rows == 1 ? 0 : rows <= 4 ? 1 : 2;
+    const int cls = rows == 1 ? 0 : 1;
     const int di = D == 128 ? 1 : 0;
     int n = cache[dev][cls][di].load(std::memory_order_relaxed);
     if (n > 0) return n;
@@ -606,14 +929,9 @@ int decode_ctas_per_sm(int rows, int D) {
     if (cls == 0)
         n = di ? resident_ctas(fa_decode_split_kernel<T, 4, 1>, sizeof(float) * kDecWarps * 1 * (128 + 2))
                : resident_ctas(fa_decode_split_kernel<T, 2, 1>, sizeof(float) * kDecWarps * 1 * (64 + 2));
-    else if (cls == 1)
-        n = di ? resident_ctas(fa_decode_rows_kernel<T, 128>, sizeof(float) * kDecWarps * 2 * 4 * (128 + 2))
-               : resident_ctas(fa_decode_rows_kernel<T, 64>, sizeof(float) * kDecWarps * 4 * 4 * (64 + 2));
     else
-        n = di ? resident_ctas(fa_decode_split_kernel<T, 4, kDecodeMaxQ>,
-                               sizeof(float) * kDecWarps * kDecodeMaxQ * (128 + 2))
-               : resident_ctas(fa_decode_split_kernel<T, 2, kDecodeMaxQ>,
-                               sizeof(float) * kDecWarps * kDecodeMaxQ * (64 + 2));
+        n = di ? resident_ctas(fa_decode_mma_kernel<T, 128>, mmadec::Cfg<128>::kSmem)
+               : resident_ctas(fa_decode_mma_kernel<T, 64>, mmadec::Cfg<64>::kSmem);
     if (n > 0) cache[dev][cls][di].store(n, std::memory_order_relaxed);
     return n;
 }

@@ -540,11 +540,17 @@ def run_native(args, w, world, rank, local, pg):
     return 0
 
 
-def decode_kernel_name(rows, n_splits):
+def decode_kernel_name(rows, n_splits, dtype="bf16"):
     """The decode kernels a call runs: one query row per (b, K/V head) takes the
-    split kernel, two to four the lane-group rows kernel, more the 16-row split
+    split kernel; two to sixteen 16-bit rows the tensor-core (mma.sync) kernel;
+    fp32 rows the lane-group rows kernel (up to four) or the 16-row split
     kernel; a combine pass follows when the cache is split."""
-    main = "fa_decode_split_kernel" if rows == 1 or rows > 4 else "fa_decode_rows_kernel"
+    if rows == 1:
+        main = "fa_decode_split_kernel"
+    elif dtype in ("f16", "bf16"):
+        main = "fa_decode_mma_kernel"
+    else:
+        main = "fa_decode_rows_kernel" if rows <= 4 else "fa_decode_split_kernel"
     return main + (" + fa_decode_combine_kernel" if n_splits > 1 else "")
 
 
@@ -615,7 +621,7 @@ def run_decode(args, w, world, rank, local, pg):
                    "n_splits": ns, "workspace_bytes": wb,
                    "l2": "K/V cache (%d MiB) exceeds L2; no flush" % (2 * w.B * Hkv * w.Nk * w.D * e >> 20)},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "traffic": None, "kernel": decode_kernel_name(w.H // Hkv * w.Nq, ns),
+                     "traffic": None, "kernel": decode_kernel_name(w.H // Hkv * w.Nq, ns, w.dtype),
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms, "peak_source": src},
         "clocks": clk, "gpu_launches": args.steps * (2 if ns > 1 else 1),
     }
