@@ -78,7 +78,8 @@ def measured_peaks():
 
 # Sources the tensor-core forward kernel is compiled from (its own file and
 # the headers it includes): a recorded traffic figure holds while they do.
-FWD_KERNEL_SOURCES = ("fa_tc.cu", "tc_common.cuh", "ptx.cuh", "fa_geom.h", "fa_internal.h")
+FWD_KERNEL_SOURCES = ("fa_tc.cu", "tc_softmax.cuh", "rope_math.cuh", "tc_common.cuh", "ptx.cuh", "fa_geom.h",
+                      "fa_internal.h")
 
 
 def kernel_source_hash(files=FWD_KERNEL_SOURCES):
