@@ -335,6 +335,7 @@ def time_forward_workload(w, args, device, pg, rank, local, peak):
             "window": [w.win_l, w.win_r], "input_scale": w.input_scale, "steps": args.also_steps,
             "avg_launch_ms": ms, "algorithmic_flops_per_launch": flops, "TFLOP/s": tf,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "traffic": recorded_traffic(w.name),
                          "kernel": "fa_fwd_tc_kernel<%d,%s>" % (w.D, w.dtype)},
             "clocks": clk}
 
