@@ -356,7 +356,8 @@ int fa_decode_plan_gqa(int B, int H, int H_kv, int Nq, int Nk, int D, int n_spli
     if (rc != FA_OK) return rc;
     int ns, chunk;
     const long long groups = (long long)B * H_kv;
-    fa::decode_plan(groups, Nk, dev->sms, n_splits, &ns, &chunk, fa::decode_ctas_per_sm((H / H_kv) * Nq, D));
+    fa::decode_plan(groups, Nk, dev->sms, n_splits, &ns, &chunk, fa::decode_ctas_per_sm((H / H_kv) * Nq, D),
+                    (H / H_kv) * Nq > 1);
     if (n_splits_out) *n_splits_out = ns;
     if (workspace_bytes) *workspace_bytes = fa::decode_workspace_bytes(groups, (H / H_kv) * Nq, D, ns);
     return FA_OK;
@@ -392,7 +393,8 @@ int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* l
     p.G = G;
     p.Hkv = H_kv;
     p.layout = layout;
-    fa::decode_plan(p.BH, Nk, dev->sms, n_splits, &p.n_splits, &p.chunk, fa::decode_ctas_per_sm(G * Nq, D));
+    fa::decode_plan(p.BH, Nk, dev->sms, n_splits, &p.n_splits, &p.chunk, fa::decode_ctas_per_sm(G * Nq, D),
+                    G * Nq > 1);
     const unsigned long long need = fa::decode_workspace_bytes(p.BH, G * Nq, D, p.n_splits);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return FA_ERR_ARG;
@@ -447,7 +449,8 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
     p.G = G;
     p.Hkv = H_kv;
     p.layout = layout;
-    fa::decode_plan(p.BH, max_seq_len, dev->sms, n_splits, &p.n_splits, &p.chunk, fa::decode_ctas_per_sm(G * Nq, D));
+    fa::decode_plan(p.BH, max_seq_len, dev->sms, n_splits, &p.n_splits, &p.chunk,
+                    fa::decode_ctas_per_sm(G * Nq, D), G * Nq > 1);
     const unsigned long long need = fa::decode_workspace_bytes(p.BH, G * Nq, D, p.n_splits);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return FA_ERR_ARG;

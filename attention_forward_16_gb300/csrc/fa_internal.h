@@ -99,22 +99,41 @@ struct DecodeParams {
 // Split count and key chunk for a decode problem (n_req <= 0: choose).
 //
 // With ctas_per_sm > 0 (the decode kernel's resident CTAs per SM, so one wave
-// is ctas_per_sm * sms CTAs) the choice is the split count, at most two waves'
-// worth, whose last wave is fullest (ties to fewer splits).  With
-// ctas_per_sm == 0 it is the older rule of about eight CTAs per SM.
-inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk, int ctas_per_sm = 0) {
+// is ctas_per_sm * sms CTAs) the choice is the split count, at most two
+// waves' worth, whose last wave is fullest; ties go to fewer splits.  With
+// one_wave_first (the tensor-core kernel, whose CTAs carry a larger fixed
+// cost: Q fragments, ring fill, merge) the split count whose single wave is
+// fullest wins instead whenever that wave is at least kDecodeOneWaveFill full:
+// every CTA of a second wave pays the fixed cost again, and for that kernel a
+// wave 84% full measured faster than two waves 98% full, while the one-row
+// kernel, with more and lighter CTAs, measured faster with two full waves.
+// With ctas_per_sm == 0 it is the older rule of about eight CTAs per SM.
+constexpr double kDecodeOneWaveFill = 0.75;
+inline void decode_plan(long long BH, int Nk, int sms, int n_req, int* n_splits, int* chunk, int ctas_per_sm = 0,
+                        bool one_wave_first = false) {
     const long long cap = (Nk + kDecodeMinKeysPerSplit - 1) / kDecodeMinKeysPerSplit;
     long long s = n_req > 0 ? n_req : (8LL * sms + BH - 1) / BH;
     if (n_req <= 0 && ctas_per_sm > 0) {
         const long long slots = (long long)ctas_per_sm * sms;
         long long best = 1;
         double best_eff = -1.0;
-        for (long long t = 1; t <= cap && BH * t <= 2 * slots; ++t) {
-            const long long waves = (BH * t + slots - 1) / slots;
-            const double eff = (double)(BH * t) / (double)(waves * slots);
+        for (long long t = 1; one_wave_first && t <= cap && BH * t <= slots; ++t) {
+            const double eff = (double)(BH * t) / (double)slots;
             if (eff > best_eff + 1e-9) {
                 best_eff = eff;
                 best = t;
+            }
+        }
+        if (best_eff < kDecodeOneWaveFill) {
+            best = 1;
+            best_eff = -1.0;
+            for (long long t = 1; t <= cap && BH * t <= 2 * slots; ++t) {
+                const long long waves = (BH * t + slots - 1) / slots;
+                const double eff = (double)(BH * t) / (double)(waves * slots);
+                if (eff > best_eff + 1e-9) {
+                    best_eff = eff;
+                    best = t;
+                }
             }
         }
         s = best;

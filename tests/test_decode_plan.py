@@ -6,6 +6,8 @@ contract.
 - With the kernel's residency given (CTAs per SM), the automatic plan takes at
   most two waves of CTAs and no admissible split count fills its last wave
   better; ties go to fewer splits; never more than ceil(Nk / 256) splits.
+  With one-wave-first (the multi-row tensor-core kernel) the split count that
+  fills one wave best wins when that wave is at least 75% full.
 - Without a residency (0) it keeps the older target of about eight CTAs per
   SM, the rule the allocation-free decode entry point uses.
 """
@@ -25,11 +27,11 @@ DRIVER = r"""
 #include <cstdlib>
 #include "fa_internal.h"
 int main(int argc, char** argv) {
-    // each line of stdin: BH Nk sms n_req ctas_per_sm
-    long long BH; int Nk, sms, req, cps;
-    while (std::scanf("%lld %d %d %d %d", &BH, &Nk, &sms, &req, &cps) == 5) {
+    // each line of stdin: BH Nk sms n_req ctas_per_sm one_wave_first
+    long long BH; int Nk, sms, req, cps, ow;
+    while (std::scanf("%lld %d %d %d %d %d", &BH, &Nk, &sms, &req, &cps, &ow) == 6) {
         int ns = 0, chunk = 0;
-        fa::decode_plan(BH, Nk, sms, req, &ns, &chunk, cps);
+        fa::decode_plan(BH, Nk, sms, req, &ns, &chunk, cps, ow != 0);
         std::printf("%d %d\n", ns, chunk);
     }
     return 0;
@@ -37,20 +39,24 @@ int main(int argc, char** argv) {
 """
 
 CASES = [
-    # (BH, Nk, sms, n_req, ctas_per_sm)
-    (64, 32768, 152, 0, 3),      # grouped-head decode, lane-group kernel
-    (256, 32768, 152, 0, 12),    # one query row per head, split kernel
-    (128, 4096, 152, 0, 3),      # four new tokens per head
-    (64, 32768, 152, 0, 0),      # the older rule
-    (1, 1, 152, 0, 3),
-    (1, 300, 152, 0, 3),
-    (4, 7, 152, 0, 3),
-    (2, 3000, 148, 0, 5),
-    (8, 65536, 152, 0, 1),
-    (5000, 4096, 152, 0, 3),     # more (b, h) than a wave: no split
-    (1, 5000, 152, 4, 3),        # explicit request wins
-    (2, 3000, 148, 100, 3),
-    (1, 65536, 152, 300, 0),
+    # (BH, Nk, sms, n_req, ctas_per_sm, one_wave_first)
+    (64, 32768, 152, 0, 3, 1),      # grouped-head decode, tensor-core kernel
+    (64, 32768, 152, 0, 3, 0),      # the same without the one-wave preference
+    (256, 32768, 152, 0, 12, 0),    # one query row per head, split kernel
+    (256, 32768, 152, 0, 16, 0),
+    (128, 4096, 152, 0, 3, 1),      # four new tokens per head
+    (128, 4096, 152, 0, 3, 0),
+    (64, 32768, 152, 0, 0, 0),      # the older rule
+    (1, 1, 152, 0, 3, 1),
+    (1, 300, 152, 0, 3, 1),
+    (4, 7, 152, 0, 3, 0),
+    (2, 3000, 148, 0, 5, 1),
+    (8, 65536, 152, 0, 1, 0),
+    (100, 65536, 152, 0, 3, 1),     # no single wave fills 75%: the two-wave rule
+    (5000, 4096, 152, 0, 3, 1),     # more (b, h) than a wave: no split
+    (1, 5000, 152, 4, 3, 1),        # explicit request wins
+    (2, 3000, 148, 100, 3, 0),
+    (1, 65536, 152, 300, 0, 0),
 ]
 
 
@@ -80,20 +86,25 @@ def _eff(BH, t, slots):
 
 
 def test_every_plan_covers_the_keys_once(plan_exe):
-    for (BH, Nk, sms, req, cps), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
+    for (BH, Nk, sms, req, cps, ow), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
         assert ns >= 1 and chunk % 4 == 0
         assert (ns - 1) * chunk < Nk <= ns * chunk, (BH, Nk, ns, chunk)
 
 
 def test_residency_plan_fills_its_last_wave_best(plan_exe):
-    for (BH, Nk, sms, req, cps), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
+    for (BH, Nk, sms, req, cps, ow), (ns, chunk) in zip(CASES, _plans(plan_exe, CASES)):
         if req > 0 or cps == 0:
             continue
         slots = cps * sms
         cap = -(-Nk // 256)
-        admissible = [t for t in range(1, cap + 1) if BH * t <= 2 * slots] or [1]
-        best = max(_eff(BH, t, slots) for t in admissible)
-        first_best = min(t for t in admissible if _eff(BH, t, slots) >= best - 1e-9)
+        one_wave = [t for t in range(1, cap + 1) if BH * t <= slots]
+        if ow and one_wave and max(BH * t / slots for t in one_wave) >= 0.75:
+            best = max(BH * t / slots for t in one_wave)
+            first_best = min(t for t in one_wave if BH * t / slots >= best - 1e-9)
+        else:
+            admissible = [t for t in range(1, cap + 1) if BH * t <= 2 * slots] or [1]
+            best = max(_eff(BH, t, slots) for t in admissible)
+            first_best = min(t for t in admissible if _eff(BH, t, slots) >= best - 1e-9)
         # the planner's count, before chunk rounding, is the first best one
         c = -(-Nk // first_best)
         c = -(-c // 4) * 4
@@ -103,13 +114,16 @@ def test_residency_plan_fills_its_last_wave_best(plan_exe):
 
 
 def test_bench_shapes_get_one_wave(plan_exe):
-    cases = [(64, 32768, 152, 0, 3), (256, 32768, 152, 0, 12), (128, 4096, 152, 0, 3)]
-    assert [p[0] for p in _plans(plan_exe, cases)] == [7, 7, 7]
+    # grouped heads and one row per head fill one wave with 7 splits; four new
+    # tokens per head (128 groups, 4k cache) take 3 splits, one wave 84% full,
+    # which measured faster (0.706 of HBM) than 7 splits in two waves (0.663)
+    cases = [(64, 32768, 152, 0, 3, 1), (256, 32768, 152, 0, 12, 0), (128, 4096, 152, 0, 3, 1)]
+    assert [p[0] for p in _plans(plan_exe, cases)] == [7, 7, 3]
 
 
 def test_zero_residency_keeps_the_older_rule(plan_exe):
     for BH, Nk, sms in [(64, 32768, 152), (8, 32768, 152), (256, 4096, 152), (2, 3000, 148)]:
-        (ns, chunk), = _plans(plan_exe, [(BH, Nk, sms, 0, 0)])
+        (ns, chunk), = _plans(plan_exe, [(BH, Nk, sms, 0, 0, 0)])
         s = -(-8 * sms // BH)
         s = max(1, min(s, -(-Nk // 256), Nk, 1024))
         c = -(-Nk // s)
@@ -118,5 +132,5 @@ def test_zero_residency_keeps_the_older_rule(plan_exe):
 
 
 def test_explicit_request_is_kept(plan_exe):
-    (ns, chunk), = _plans(plan_exe, [(1, 5000, 152, 4, 3)])
+    (ns, chunk), = _plans(plan_exe, [(1, 5000, 152, 4, 3, 1)])
     assert ns == 4 and chunk == 1252
