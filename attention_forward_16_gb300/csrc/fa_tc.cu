@@ -74,7 +74,9 @@ struct TcCfg {
     static constexpr int kColO0 = 256;
     static constexpr int kColO1 = 256 + D;
     static constexpr int kTmemCols = 512;
-    static constexpr int kTileSmem = (2 + kStages) * kTileBytes;
+    // Q tiles, the K/V ring, and one 64-column O staging box per Q tile for
+    // the epilogue's TMA stores.
+    static constexpr int kTileSmem = (2 + kStages) * kTileBytes + 2 * kBoxBytes;
 };
 
 struct __align__(16) SharedCtl {
@@ -84,6 +86,7 @@ struct __align__(16) SharedCtl {
     uint64_t s_full[2][2], p_full[2][2];  // per Q tile and S half
     uint64_t pv_done[2][2];               // per Q tile: P.V products completed, by step parity
     uint64_t o_done[2], o_free[2];
+    uint64_t stg_full[2], stg_free[2];    // per Q tile: O staging box written / read by its TMA store
     uint64_t drain[2];
     uint32_t tmem_base;
     int abort;
@@ -334,7 +337,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
 // ------------------------------------------------------ softmax + epilogue
 template <int D, bool kBf16, bool kPosScale>
 __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t tmem,
-                                             uint8_t* sQ, int warp, int lane) {
+                                             uint8_t* sQ, uint32_t sStg, int warp, int lane) {
     using C = TcCfg<D>;
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -347,6 +350,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     const float c2 = p.scale_log2;
     uint32_t s_cnt[2] = {0, 0};
     uint32_t u_cnt = 0, q_cnt = 0, g = 0;  // g: S halves taken so far (P.V steps)
+    uint32_t e_cnt = 0;                    // O chunks staged so far
     bool ok = true;
     for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
         const Unit un = make_unit(p.g, p.BH, p.order, u);
@@ -399,35 +403,73 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
         tc_fence_after();
         const float inv = 1.f / l;
         const bool live = qi < p.g.N;
-        const size_t orow = (size_t)row_index(p.layout, un.bh / p.H, un.bh % p.H, live ? qi : 0, p.H, p.g.N);
         const size_t lrow = (size_t)un.bh * p.g.N + (size_t)(live ? qi : 0);
+        if (p.o_f32) {
+            const size_t orow = (size_t)row_index(p.layout, un.bh / p.H, un.bh % p.H, live ? qi : 0, p.H, p.g.N);
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_wait_ld();
-            if (live) {
-                if (p.o_f32) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_wait_ld();
+                if (live) {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * D + c * 32);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         dst[i] = make_float4(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv, u2f(o[4 * i + 2]) * inv,
                                              u2f(o[4 * i + 3]) * inv);
-                } else {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pack2<kBf16>(u2f(o[8 * i]) * inv, u2f(o[8 * i + 1]) * inv),
-                                            pack2<kBf16>(u2f(o[8 * i + 2]) * inv, u2f(o[8 * i + 3]) * inv),
-                                            pack2<kBf16>(u2f(o[8 * i + 4]) * inv, u2f(o[8 * i + 5]) * inv),
-                                            pack2<kBf16>(u2f(o[8 * i + 6]) * inv, u2f(o[8 * i + 7]) * inv));
                 }
             }
+            tc_fence_before();
+            mbar_arrive(o_free);
+        } else {
+            // 16-bit O: each 64-column chunk goes through this tile's staging
+            // box (128-byte swizzled rows, the layout of the O tensor map) and
+            // one TMA store, so the write-back is whole-box copies rather than
+            // 16-byte stores that touch a cache line per row.  The O columns
+            // are released to the next unit's P.V as soon as the last chunk
+            // has been read out of TMEM.
+            const uint32_t stg = sStg + t * C::kBoxBytes;
+            const uint32_t stg_full = smem_u32(&sh->stg_full[t]);
+            const uint32_t stg_free = smem_u32(&sh->stg_free[t]);
+            const bool issuer = row == 0;
+#pragma unroll 1
+            for (int c = 0; c < D / 64 && ok; ++c) {
+                uint32_t oa[32], ob[32];
+                tmem_ld32(tO + c * 64, oa);
+                tmem_ld32(tO + c * 64 + 32, ob);
+                tmem_wait_ld();
+                if (c == D / 64 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(o_free);
+                }
+                // the previous store out of this box has read it
+                if (e_cnt > 0 && !(ok = W.wait_warp(stg_free, (e_cnt - 1) & 1))) break;
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    const uint32_t* w = uu < 4 ? oa + 8 * uu : ob + 8 * (uu - 4);
+                    const uint4 v = make_uint4(pack2<kBf16>(u2f(w[0]) * inv, u2f(w[1]) * inv),
+                                               pack2<kBf16>(u2f(w[2]) * inv, u2f(w[3]) * inv),
+                                               pack2<kBf16>(u2f(w[4]) * inv, u2f(w[5]) * inv),
+                                               pack2<kBf16>(u2f(w[6]) * inv, u2f(w[7]) * inv));
+                    st_shared_v4(stg + row * 128 + (((uint32_t)uu ^ (uint32_t)(row & 7)) << 4), v);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(stg_full);
+                if (issuer && (ok = W.wait(stg_full, e_cnt & 1))) {
+                    tma_store_5d(&p.tm_o, stg, 0, r0, c, un.bh % p.H, un.bh / p.H);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(stg_free);
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                ++e_cnt;
+            }
+            if (!ok) break;
         }
         if (live && p.lse) p.lse[lrow] = (m_ref + log2f(l)) * kLn2;
-        tc_fence_before();
-        mbar_arrive(o_free);
     }
+    // Every TMA store of O has finished before the CTA's shared memory goes.
+    if (row == 0) bulk_wait_group<0>();
 }
 
 template <int D, bool kBf16, bool kPosScale>
@@ -461,6 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
             }
             mbar_init(smem_u32(&sh->o_done[t]), 1);
             mbar_init(smem_u32(&sh->o_free[t]), 128);
+            mbar_init(smem_u32(&sh->stg_full[t]), 128);
+            mbar_init(smem_u32(&sh->stg_free[t]), 1);
         }
         mbar_init(smem_u32(&sh->drain[0]), 1);
         mbar_init(smem_u32(&sh->drain[1]), 1);
@@ -485,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
         setmaxnreg_inc<kRegSoftmax>();
 
     if (warp < 8) {
-        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, smem, warp, lane);
+        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, smem, sKVa + C::kStages * C::kTileBytes, warp, lane);
     } else if (warp == kWarpMma || warp == kWarpMma1) {
         mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
     } else if (warp == kWarpTma) {
