@@ -246,8 +246,9 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
         const int clusters = p.n_units < dev->sms / 2 ? p.n_units : dev->sms / 2;
         e = fa::launch_tc_pair(p, bf16, scale > 0.f, clusters, s);
     } else {
-        const int grid = p.n_units < dev->sms ? p.n_units : dev->sms;
-        e = fa::launch_tc(p, D, bf16, scale > 0.f, grid, s);
+        // One CTA per unit: the CTAs that run take the units of those that
+        // have not started yet (cluster launch control), so as many run as fit.
+        e = fa::launch_tc(p, D, bf16, scale > 0.f, p.n_units, s);
     }
     return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }

@@ -79,7 +79,14 @@ struct TcCfg {
     static constexpr int kTileSmem = (2 + kStages) * kTileBytes + 2 * kBoxBytes;
 };
 
+constexpr int kUnitRing = 4;  // unit indices handed from the scheduler to the other roles
+constexpr int kUnitReaders = 1 + 32 + 32 + 128 + 128;  // K/V thread, two MMA warps, two softmax warpgroups
+
 struct __align__(16) SharedCtl {
+    uint4 clc_resp;                  // cluster launch control answer (16-byte aligned)
+    int unit_ring[kUnitRing];
+    uint64_t u_full[kUnitRing], u_empty[kUnitRing];
+    uint64_t clc_bar;
     uint64_t q_full[2], q_empty[2];  // per Q tile
     uint64_t q_ready[2];             // per Q tile: rotated in place (rotary embedding of Q)
     uint64_t kv_full[8], kv_empty[8];
@@ -113,6 +120,17 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, u
     tma_load_5d(dst, tm, bar, 0, row, 0, head, b);
 }
 
+// Units are handed out dynamically.  The grid has one CTA per unit, and one
+// CTA fits an SM, so 152 run at a time.  A running CTA first takes its own
+// unit, then takes each further unit from a CTA of the grid that has not
+// started yet: it cancels that CTA's launch with cluster launch control, and
+// the cancelled CTA never runs.  CTAs start in index order and units are
+// numbered longest first, so faster SMs take more units and every CTA ends
+// close to the others (the static round-robin of units left SMs that ran
+// slower 10% behind).  The Q thread is the scheduler: it publishes each unit
+// index (then -1) into a small ring that every other role reads in order,
+// and requests the next index while it loads the current unit's Q.
+//
 // Q tiles: one thread, one buffer per tile.  Tile t of the next unit is loaded
 // as soon as tile t's last S of the current unit has completed, so a tile that
 // finishes its key range first (tile 0 under causal and window masks) can
@@ -123,8 +141,23 @@ __device__ __forceinline__ void tma_q_role(const TcParams& p, const Waiter& W, S
     using C = TcCfg<D>;
     tma_prefetch_desc(&p.tm_q);
     uint32_t q_it[2] = {0, 0};
+    const uint32_t clc_bar = smem_u32(&sh->clc_bar);
+    const uint32_t resp = smem_u32(&sh->clc_resp);
+    uint32_t asked = 0;  // cancel requests issued (each completes one phase of clc_bar)
     bool ok = true;
-    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
+    int u = blockIdx.x;
+    for (uint32_t k = 0; ok; ++k) {
+        const uint32_t slot = k % kUnitRing;
+        if (k >= (uint32_t)kUnitRing && !(ok = W.wait(smem_u32(&sh->u_empty[slot]), (k / kUnitRing - 1) & 1)))
+            break;
+        sh->unit_ring[slot] = u;
+        mbar_arrive(smem_u32(&sh->u_full[slot]));
+        if (u < 0) break;
+        // the next unit, asked for now so that the answer is back by the time
+        // this unit's Q is on its way
+        mbar_arrive_expect_tx(clc_bar, 16);
+        clc_try_cancel(resp, clc_bar);
+        ++asked;
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         const int b = un.bh / p.H, h = un.bh % p.H;
         for (int t = 0; t < 2 && ok; ++t) {
@@ -134,19 +167,36 @@ __device__ __forceinline__ void tma_q_role(const TcParams& p, const Waiter& W, S
             load_tile(sQa + t * C::kTileBytes, &p.tm_q, q_full, un.q0 + t * kTileM, h, b);
             ++q_it[t];
         }
-        // Pull this CTA's next Q tiles into L2 now: their loads wait for this
+        if (!ok || !(ok = W.wait(clc_bar, (asked - 1) & 1))) break;
+        u = clc_query(resp);
+        // Pull the next unit's Q tiles into L2 now: their loads wait for this
         // unit's last S products, and would otherwise start with a DRAM latency.
-        const int un_next = sched_unit(r + 1, blockIdx.x, gridDim.x);
-        if (ok && un_next < p.n_units) {
-            const Unit nx = make_unit(p.g, p.BH, p.order, un_next);
+        if (u >= 0) {
+            const Unit nx = make_unit(p.g, p.BH, p.order, u);
             const int nb = nx.bh / p.H, nh = nx.bh % p.H;
             for (int t = 0; t < 2; ++t) tma_prefetch_l2_5d(&p.tm_q, 0, nx.q0 + t * kTileM, 0, nh, nb);
         }
     }
-    // Let every issued copy land before shared memory is released (on the
-    // normal path too: after an abort elsewhere nobody may wait for them).
+    // Let every issued copy (and an answer still on its way) land before
+    // shared memory is released (on the normal path too: after an abort
+    // elsewhere nobody may wait for them).
     for (int t = 0; t < 2; ++t)
         if (q_it[t] > 0) W.drain(smem_u32(&sh->q_full[t]), (q_it[t] - 1) & 1);
+    if (asked > 0) W.drain(clc_bar, (asked - 1) & 1);
+}
+
+// The next unit index for a role other than the scheduler (-1: no more), read
+// from ring position k; every reading thread then frees its slot.  Warp-
+// uniform when kWarp (every lane waits and reads).
+template <bool kWarp>
+__device__ __forceinline__ int next_unit(SharedCtl* sh, const Waiter& W, uint32_t k, bool& ok) {
+    const uint32_t slot = k % kUnitRing;
+    const uint32_t full = smem_u32(&sh->u_full[slot]);
+    ok = kWarp ? W.wait_warp(full, (k / kUnitRing) & 1) : W.wait(full, (k / kUnitRing) & 1);
+    if (!ok) return -1;
+    const int u = *reinterpret_cast<volatile int*>(&sh->unit_ring[slot]);
+    mbar_arrive(smem_u32(&sh->u_empty[slot]));
+    return u;
 }
 
 // K/V tiles: one thread filling the ring, K_j then V_j for every key tile in
@@ -158,7 +208,9 @@ __device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, 
     tma_prefetch_desc(&p.tm_v);
     uint32_t kv_it = 0;
     bool ok = true;
-    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
+    for (uint32_t r = 0; ok; ++r) {
+        const int u = next_unit<false>(sh, W, r, ok);
+        if (u < 0) break;
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         const int b = un.bh / p.H, h = un.bh % p.H, hk = h / p.G;
         for (int j = un.jlo; j < un.jhi && ok; ++j) {
@@ -274,7 +326,9 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         return true;
     };
 
-    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
+    for (uint32_t r = 0; ok; ++r) {
+        const int u = next_unit<true>(sh, W, r, ok);
+        if (u < 0) break;
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         if (!(ok = W.wait_warp(q_full, q_it & 1))) break;
         ++q_it;
@@ -352,7 +406,9 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     uint32_t u_cnt = 0, q_cnt = 0, g = 0;  // g: S halves taken so far (P.V steps)
     uint32_t e_cnt = 0;                    // O chunks staged so far
     bool ok = true;
-    for (int r = 0, u; (u = sched_unit(r, blockIdx.x, gridDim.x)) < p.n_units && ok; ++r) {
+    for (uint32_t r = 0; ok; ++r) {
+        const int u = next_unit<true>(sh, W, r, ok);
+        if (u < 0) break;
         const Unit un = make_unit(p.g, p.BH, p.order, u);
         const int jlo_t = t ? un.lo[1] : un.lo[0];
         const int jhi_t = t ? un.hi[1] : un.hi[0];
@@ -508,6 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
         }
         mbar_init(smem_u32(&sh->drain[0]), 1);
         mbar_init(smem_u32(&sh->drain[1]), 1);
+        for (int k = 0; k < kUnitRing; ++k) {
+            mbar_init(smem_u32(&sh->u_full[k]), 1);
+            mbar_init(smem_u32(&sh->u_empty[k]), kUnitReaders);
+        }
+        mbar_init(smem_u32(&sh->clc_bar), 1);
         sh->abort = 0;
         fence_mbar_init();
         fence_proxy_async_smem();

@@ -120,6 +120,31 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// ------------------------------------------------- cluster launch control
+// Ask the hardware to cancel the launch of a CTA of this grid that has not
+// started yet and hand its index to the caller (the 16-byte answer lands at
+// `resp` and completes 16 transaction bytes on `bar`).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     resp),
+                 "r"(bar)
+                 : "memory");
+}
+// The x index of the CTA whose launch the answer at `resp` cancelled, or -1
+// if the request failed (no CTA of the grid was left to cancel).
+__device__ __forceinline__ int clc_query(uint32_t resp) {
+    int x = -1;
+    asm volatile(
+        "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 h, [%1];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, h;\n\t}"
+        : "+r"(x)
+        : "r"(resp)
+        : "memory");
+    return x;
+}
+
 // 16 bytes to shared memory at a shared-space address.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

@@ -433,7 +433,9 @@ int fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 /*
  * fa_plan_units -- host-side view of the work decomposition the tensor-core
  * kernel uses (no GPU needed).  Units are pairs of 128-row query tiles of one
- * (b, h), in the order persistent CTAs take them.  If `out` is not NULL,
+ * (b, h), in the order the kernel hands them out (longest first where their
+ * lengths differ; the CTAs that run take the next unit as they become free).
+ * If `out` is not NULL,
  * writes min(cap, n_units) records of 6 ints {bh, q0, lo0, hi0, lo1, hi1}:
  * query rows [q0, q0+128) visit key tiles [lo0, hi0), rows [q0+128, q0+256)
  * visit [lo1, hi1) (key tile j = keys [128 j, 128 j + 128)); lo == hi marks a
