@@ -143,6 +143,25 @@ def test_unit_order_is_longest_first_for_causal(lib):
     assert work == sorted(work, reverse=True)
 
 
+def test_causal_units_come_in_head_groups(lib):
+    # N = 4096: groups of 32 heads (a group's K/V, 2 MB a head, fits half of
+    # L2), each group longest first; 4 x 32 = 128 heads make four groups, the
+    # last one short when the heads do not divide evenly
+    for B, H in ((4, 32), (3, 25)):
+        units = fb.fa_plan_units(B, H, 4096, MASK_CAUSAL)
+        BH, per_head = B * H, 16
+        assert len(units) == BH * per_head
+        start = 0
+        for g0 in range(0, BH, 32):
+            gh = min(32, BH - g0)
+            grp = units[start:start + gh * per_head]
+            start += gh * per_head
+            assert {u[0] for u in grp} == set(range(g0, g0 + gh))
+            work = [(hi0 - lo0) + (hi1 - lo1) for (_, _, lo0, hi0, lo1, hi1) in grp]
+            assert work == sorted(work, reverse=True)
+        assert start == len(units)
+
+
 # ------------------------------------------------------------- FLOP count
 
 @pytest.mark.parametrize("N", [1, 2, 7, 128, 129, 1000])
