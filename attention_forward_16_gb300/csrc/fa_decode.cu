@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const Deco
     using V = Vec<T, DV>;
     constexpr int D = 32 * DV;
     extern __shared__ float dsm[];  // [warps][NQ][D + 2]: m, l, acc
+    ptx::griddep_launch_dependents();    // the combine pass may start launching
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.n_splits;
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_rows_kernel(const Decod
     constexpr int kStates = kDecWarps * KPW;
     constexpr int DV = D / 32;
     extern __shared__ float dsm[];                  // [kStates][4][D + 2]: m, l, acc
+    ptx::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int grp = lane / L;
@@ -606,6 +608,7 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_mma_kernel(const Decode
     using C = Cfg<D>;
     constexpr float kTauDec = 8.0f;  // lazy rescale threshold (log2 units), as in the forward
     extern __shared__ __align__(128) uint8_t dec_smem[];
+    ptx::griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;  // fragment row (and row + 8)
@@ -812,10 +815,13 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_mma_kernel(const Decode
 }
 
 
-// One warp per output row: O = sum_s e^{LSE_s - LSE} O_s.
+// One warp per output row: O = sum_s e^{LSE_s - LSE} O_s.  It is launched as a
+// programmatic dependent of the split pass, so its CTAs can be resident before
+// that pass ends; griddep_wait holds them until the partials are written.
 template <typename T, int DV>
 __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const DecodeParams p) {
     constexpr int D = 32 * DV;
+    ptx::griddep_wait();
     const int lane = threadIdx.x & 31;
     const int rows = p.G * p.Nq;
     const long long rowid = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -900,8 +906,20 @@ cudaError_t launch_typed(const DecodeParams& p, cudaStream_t s) {
                                       : launch_split<T, DV, kDecodeMaxQ>(p, s);
     if (e != cudaSuccess || p.n_splits == 1) return e;
     const long long all_rows = (long long)p.BH * rows;
-    fa_decode_combine_kernel<T, DV><<<(unsigned)((all_rows + 3) / 4), 128, 0, s>>>(p);
-    return cudaGetLastError();
+    if ((all_rows + 3) / 4 > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // Programmatic stream serialization: the combine grid launches while the
+    // split pass drains instead of after it, hiding its launch latency.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((all_rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<T, DV>, p);
 }
 
 template <typename Kern>

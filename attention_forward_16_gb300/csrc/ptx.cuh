@@ -30,6 +30,16 @@ __device__ __forceinline__ bool elect_one() {
     return r != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream, if it was launched with programmatic stream serialization, start its
+// CTAs once every CTA of this grid has issued it or exited; wait blocks until
+// the previous grid has completed and its memory writes are visible.  Both do
+// nothing for kernels launched without the attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
