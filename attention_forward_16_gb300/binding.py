@@ -63,6 +63,7 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "fa_plan_units": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), _I]),
     "fa_tile_needs_mask": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_geom_needs_masks": (_I, [_I, _I, _I, _I]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (ctypes.c_char_p, []),
     "fa_version": (_I, []),
@@ -239,6 +240,10 @@ def fa_plan_units(B, H, N, mask_kind, win_l=-1, win_r=-1):
 
 def fa_tile_needs_mask(N, mask_kind, win_l, win_r, r0, j):
     return load().fa_tile_needs_mask(N, mask_kind, win_l, win_r, r0, j)
+
+
+def fa_geom_needs_masks(N, mask_kind, win_l, win_r):
+    return load().fa_geom_needs_masks(N, mask_kind, win_l, win_r)
 
 
 # ------------------------------------------------------------ tensor level

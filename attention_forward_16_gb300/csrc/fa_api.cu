@@ -643,6 +643,12 @@ int fa_tile_needs_mask(int N, int mask_kind, int win_l, int win_r, int r0, int j
     return fa::tile_needs_mask(g, r0, j) ? 1 : 0;
 }
 
+int fa_geom_needs_masks(int N, int mask_kind, int win_l, int win_r) {
+    fa::Geom g;
+    if (normalise_mask(mask_kind, win_l, win_r, N, &g) != FA_OK) return FA_ERR_ARG;
+    return fa::geom_needs_masks(g) ? 1 : 0;
+}
+
 const char* fa_strerror(int code) {
     switch (code) {
         case FA_OK: return "ok";

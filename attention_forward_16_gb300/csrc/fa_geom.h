@@ -140,6 +140,15 @@ FA_HD bool tile_split_p(const Geom& g, int r0) {
     return min_visible_keys(g, r0, r1) < kSplitKeys;
 }
 
+// False when no tile of the problem needs an element mask or a split P: no
+// window or causal bound, whole key tiles only (N a multiple of kTileN), and
+// every row sees all N >= kSplitKeys keys.  tile_needs_mask and tile_split_p
+// are then false everywhere, and the forward kernel can be built without
+// those paths.
+FA_HD bool geom_needs_masks(const Geom& g) {
+    return g.win_l >= 0 || g.win_r >= 0 || g.N % kTileN != 0 || g.N < kSplitKeys;
+}
+
 // One persistent work unit: two consecutive 128-row Q tiles of one (b, h).
 struct Unit {
     int bh;      // b * H + h

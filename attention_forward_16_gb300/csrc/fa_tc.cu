@@ -257,7 +257,7 @@ __device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, 
 // by adding encoded offsets (the start address field holds address / 16, and
 // every shared address here stays below 256 KiB, so the add never carries out
 // of the field).
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kMask>
 __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t sQa,
                                          uint32_t sKVa, uint32_t tmem, int t) {
     using C = TcCfg<D>;
@@ -343,7 +343,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
             for (int j = un.jlo; j < un.jhi && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
             continue;
         }
-        const bool split = kBf16 && tile_split_p(p.g, un.q0 + t * kTileM);
+        const bool split = kBf16 && kMask && tile_split_p(p.g, un.q0 + t * kTileM);
         for (int j = un.jlo; j < lo && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
         if (!ok || !(ok = wait_kv(kidx(lo)))) break;
         issue_s(kidx(lo) % C::kStages, 0);
@@ -389,7 +389,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
 }
 
 // ------------------------------------------------------ softmax + epilogue
-template <int D, bool kBf16, bool kPosScale>
+template <int D, bool kBf16, bool kPosScale, bool kMask>
 __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W, SharedCtl* sh, uint32_t tmem,
                                              uint8_t* sQ, uint32_t sStg, int warp, int lane) {
     using C = TcCfg<D>;
@@ -402,7 +402,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     const uint32_t o_done = smem_u32(&sh->o_done[t]);
     const uint32_t o_free = smem_u32(&sh->o_free[t]);
     const float c2 = p.scale_log2;
-    uint32_t s_cnt[2] = {0, 0};
+    uint32_t sc = 0;  // key tiles whose two S halves were taken
     uint32_t u_cnt = 0, q_cnt = 0, g = 0;  // g: S halves taken so far (P.V steps)
     uint32_t e_cnt = 0;                    // O chunks staged so far
     bool ok = true;
@@ -429,21 +429,25 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             mbar_arrive(smem_u32(&sh->q_ready[t]));
         }
         if (jlo_t == jhi_t) continue;
-        const bool split = kBf16 && tile_split_p(p.g, r0);
+        const bool split = kBf16 && kMask && tile_split_p(p.g, r0);
         float m_ref = -INFINITY;
         float l = 0.f;
         for (int j = jlo_t; j < jhi_t && ok; ++j) {
-#pragma unroll
+            // With masks, bf16 carries the split-P path as well: with both
+            // halves inlined its softmax code outgrows the instruction cache,
+            // so the halves share one copy there (the other builds keep the
+            // unrolled pair, which schedules better).
+#pragma unroll((kBf16 && kMask) ? 1 : 2)
             for (int h = 0; h < 2; ++h) {
-                if (!(ok = W.wait_warp(smem_u32(&sh->s_full[t][h]), s_cnt[h] & 1))) break;
-                ++s_cnt[h];
+                if (!(ok = W.wait_warp(smem_u32(&sh->s_full[t][h]), sc & 1))) break;
+                sc += (uint32_t)h;
                 tc_fence_after();
                 // The P.V of the previous half is the only product that can
                 // still be adding into O here.
                 const uint32_t gp = g - 1;
                 auto wait_pv = [&]() { return W.wait_warp(smem_u32(&sh->pv_done[t][gp & 1]), (gp >> 1) & 1); };
                 float lsum;
-                if (!(ok = softmax_half<D, kBf16, kPosScale>(p.g, tS + h * (kTileN / 2), tO, c2, r0, qi, j, h,
+                if (!(ok = softmax_half<D, kBf16, kPosScale, kMask>(p.g, tS + h * (kTileN / 2), tO, c2, r0, qi, j, h,
                                                              j == jlo_t && h == 0, split, m_ref, l, lsum, wait_pv)))
                     break;
                 mbar_arrive(smem_u32(&sh->p_full[t][h]));
@@ -498,7 +502,13 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                     tc_fence_before();
                     mbar_arrive(o_free);
                 }
-                // the previous store out of this box has read it
+                // The previous store out of this box has read it: its issuer
+                // waits for that only now, when the box is wanted again, so
+                // the wait is off the path that releases O.
+                if (issuer && e_cnt > 0) {
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(stg_free);
+                }
                 if (e_cnt > 0 && !(ok = W.wait_warp(stg_free, (e_cnt - 1) & 1))) break;
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) {
@@ -514,8 +524,6 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                 if (issuer && (ok = W.wait(stg_full, e_cnt & 1))) {
                     tma_store_5d(&p.tm_o, stg, 0, r0, c, un.bh % p.H, un.bh / p.H);
                     bulk_commit_group();
-                    bulk_wait_group_read<0>();
-                    mbar_arrive(stg_free);
                 }
                 ok = __all_sync(0xffffffffu, ok);
                 ++e_cnt;
@@ -528,7 +536,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
     if (row == 0) bulk_wait_group<0>();
 }
 
-template <int D, bool kBf16, bool kPosScale>
+template <int D, bool kBf16, bool kPosScale, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = TcCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -590,9 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
         setmaxnreg_inc<kRegSoftmax>();
 
     if (warp < 8) {
-        softmax_role<D, kBf16, kPosScale>(p, W, sh, tmem, smem, sKVa + C::kStages * C::kTileBytes, warp, lane);
+        softmax_role<D, kBf16, kPosScale, kMask>(p, W, sh, tmem, smem, sKVa + C::kStages * C::kTileBytes, warp, lane);
     } else if (warp == kWarpMma || warp == kWarpMma1) {
-        mma_role<D, kBf16>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
+        mma_role<D, kBf16, kMask>(p, W, sh, sQa, sKVa, tmem, warp == kWarpMma ? 0 : 1);
     } else if (warp == kWarpTma) {
         if (lane == 0) tma_kv_role<D>(p, W, sh, sKVa);
     } else if (warp == kWarpTmaQ) {
@@ -607,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
     }
 }
 
-template <int D, bool kBf16, bool kPos>
+template <int D, bool kBf16, bool kPos, bool kMask>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
-    auto kern = fa_fwd_tc_kernel<D, kBf16, kPos>;
+    auto kern = fa_fwd_tc_kernel<D, kBf16, kPos, kMask>;
     constexpr int smem = smem_bytes<D>();
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, kern);
@@ -623,15 +631,19 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Problems with no mask or split P anywhere (and a positive scale, the usual
+// case) take the build without those paths; every other one the full build.
+template <int D, bool kBf16>
+cudaError_t launch_dt(const TcParams& p, bool pos_scale, int grid, cudaStream_t s) {
+    if (pos_scale && !geom_needs_masks(p.g)) return launch_one<D, kBf16, true, false>(p, grid, s);
+    return pos_scale ? launch_one<D, kBf16, true, true>(p, grid, s) : launch_one<D, kBf16, false, true>(p, grid, s);
+}
+
 }  // namespace
 
 cudaError_t launch_tc(const TcParams& p, int D, bool bf16, bool pos_scale, int grid, cudaStream_t s) {
-    if (D == 128) {
-        if (bf16) return pos_scale ? launch_one<128, true, true>(p, grid, s) : launch_one<128, true, false>(p, grid, s);
-        return pos_scale ? launch_one<128, false, true>(p, grid, s) : launch_one<128, false, false>(p, grid, s);
-    }
-    if (bf16) return pos_scale ? launch_one<64, true, true>(p, grid, s) : launch_one<64, true, false>(p, grid, s);
-    return pos_scale ? launch_one<64, false, true>(p, grid, s) : launch_one<64, false, false>(p, grid, s);
+    if (D == 128) return bf16 ? launch_dt<128, true>(p, pos_scale, grid, s) : launch_dt<128, false>(p, pos_scale, grid, s);
+    return bf16 ? launch_dt<64, true>(p, pos_scale, grid, s) : launch_dt<64, false>(p, pos_scale, grid, s);
 }
 
 }  // namespace fa

@@ -45,8 +45,9 @@ __device__ __forceinline__ uint32_t span_bits(int lo, int hi) {
 // `lsum` holds this half's row sum.  When the running max moves by more than
 // kTau, O is rescaled in place after `wait_pv()` has confirmed that the
 // product still adding into O (the previous half's P.V) has completed; false
-// if that wait gave up.
-template <int D, bool kBf16, bool kPosScale, class WaitPv>
+// if that wait gave up.  kMask = false builds the step without the element
+// mask, for problems where no tile needs one (geom_needs_masks).
+template <int D, bool kBf16, bool kPosScale, bool kMask, class WaitPv>
 __device__ __forceinline__ bool softmax_half(const Geom& g, uint32_t tS, uint32_t tO, float c2, int r0, int qi, int j,
                                              int h, bool first, bool split, float& m_ref, float& l, float& lsum,
                                              const WaitPv& wait_pv) {
@@ -67,7 +68,7 @@ __device__ __forceinline__ bool softmax_half(const Geom& g, uint32_t tS, uint32_
                 s[c][i + 1] = f2u(b);
             }
     }
-    if (tile_needs_mask(g, r0, j)) {  // the same for the whole tile
+    if (kMask && tile_needs_mask(g, r0, j)) {  // the same for the whole tile
         // The row's visible interval as a bit set per 32-column chunk; a chunk
         // the whole warp sees in full is skipped.
         int c_lo, c_hi;

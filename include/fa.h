@@ -448,6 +448,12 @@ int fa_plan_units(int B, int H, int N, int mask_kind, int win_l, int win_r, int*
  * whole tile is visible, FA_ERR_ARG on a bad mask.  No GPU needed. */
 int fa_tile_needs_mask(int N, int mask_kind, int win_l, int win_r, int r0, int j);
 
+/* 1 if some tile of an N-position problem under this mask may need an element
+ * mask or a split P (a window or causal bound, N not a multiple of 128, or
+ * N < 512), 0 if none does -- the tensor-core forward then runs a build
+ * without those paths -- FA_ERR_ARG on a bad mask.  No GPU needed. */
+int fa_geom_needs_masks(int N, int mask_kind, int win_l, int win_r);
+
 /* Human-readable text for a return code. Never NULL. */
 const char* fa_strerror(int code);
 

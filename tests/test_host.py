@@ -137,6 +137,28 @@ def test_tiles_without_mask_are_fully_visible(lib, BH, N, mk, wl, wr):
                 assert block.all() and (j + 1) * 128 <= N
 
 
+@pytest.mark.parametrize("N,mk,wl,wr,expect", [
+    (512, MASK_NONE, -1, -1, 0), (4096, MASK_NONE, -1, -1, 0), (1024, MASK_WINDOW, -1, -1, 0),
+    (384, MASK_NONE, -1, -1, 1),      # rows see fewer than 512 keys: bf16 split P
+    (640 + 5, MASK_NONE, -1, -1, 1),  # ragged last key tile
+    (1024, MASK_CAUSAL, -1, -1, 1), (1024, MASK_WINDOW, 100, -1, 1), (1024, MASK_WINDOW, -1, 0, 1),
+    (1024, MASK_WINDOW, 2000, 2000, 1),
+])
+def test_unmasked_build_only_for_problems_without_masks(lib, N, mk, wl, wr, expect):
+    # The forward kernel's build without mask and split-P paths is taken only
+    # where every tile is fully visible and every row sees at least 512 keys.
+    got = fb.fa_geom_needs_masks(N, mk, wl, wr)
+    assert got == expect
+    if got == 0:
+        ok = allowed_mask(N, N, mk, wl, wr)
+        assert ok.all() and N % 128 == 0 and N >= 512
+        nt = N // 128
+        for r0 in range(0, N, 128):
+            for j in range(nt):
+                assert fb.fa_tile_needs_mask(N, mk, wl, wr, r0, j) == 0
+    assert fb.fa_geom_needs_masks(N, 7, wl, wr) < 0  # bad mask kind
+
+
 def test_unit_order_is_longest_first_for_causal(lib):
     units = fb.fa_plan_units(2, 3, 1024, MASK_CAUSAL)
     work = [(hi0 - lo0) + (hi1 - lo1) for (_, _, lo0, hi0, lo1, hi1) in units]
