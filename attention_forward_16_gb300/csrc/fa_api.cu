@@ -217,7 +217,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     if ((rc = make_tile_map(&p.tm_v, v, bf16, layout, B, H_kv, N, D, fa::kTileN, pair ? 1 : chunks)) != FA_OK)
         return rc;
     // 16-bit O leaves the one-CTA kernel by TMA stores of 64-column boxes
-    if (o_dtype != FA_F32 && (rc = make_tile_map(&p.tm_o, o, bf16, layout, B, H, N, D, fa::kTileM, 1)) != FA_OK)
+    if (o_dtype != FA_F32 && (rc = make_tile_map(&p.tm_o, o, bf16, layout, B, H, N, D, 32, 1)) != FA_OK)
         return rc;
     p.o = o;
     p.lse = lse;

@@ -25,8 +25,9 @@ struct TcParams {
     CUtensorMap tm_q;   // 5-D maps {64 columns, rows, D/64 chunks, heads, batch} of either layout,
     CUtensorMap tm_k;   // 16-bit, 128-byte swizzle; one box is a whole tile (all chunks of
     CUtensorMap tm_v;   // 128 rows; the pair kernel's K and V halves: see launch_tc_pair)
-    CUtensorMap tm_o;   // O with Q's map shape, box 64 columns x 128 rows: the one-CTA kernel's
-                        // epilogue stores 16-bit O through it (unused for fp32 O)
+    CUtensorMap tm_o;   // O with Q's map shape, box 64 columns x 32 rows: each softmax warp of
+                        // the one-CTA kernel stores its rows of 16-bit O through it (unused
+                        // for fp32 O)
     void* o;            // O in Q's layout, 16-bit or fp32 (o_f32)
     float* lse;         // [B, H, N] or null
     Geom g;

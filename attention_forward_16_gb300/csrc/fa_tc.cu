@@ -93,7 +93,6 @@ struct __align__(16) SharedCtl {
     uint64_t s_full[2][2], p_full[2][2];  // per Q tile and S half
     uint64_t pv_done[2][2];               // per Q tile: P.V products completed, by step parity
     uint64_t o_done[2], o_free[2];
-    uint64_t stg_full[2], stg_free[2];    // per Q tile: O staging box written / read by its TMA store
     uint64_t drain[2];
     uint32_t tmem_base;
     int abort;
@@ -482,18 +481,18 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
             tc_fence_before();
             mbar_arrive(o_free);
         } else {
-            // 16-bit O: each 64-column chunk goes through this tile's staging
-            // box (128-byte swizzled rows, the layout of the O tensor map) and
-            // one TMA store, so the write-back is whole-box copies rather than
-            // 16-byte stores that touch a cache line per row.  The O columns
+            // 16-bit O: each warp stages its 32 rows of a 64-column chunk in
+            // its own quarter of the tile's box (128-byte swizzled rows, the
+            // layout of the O tensor map) and writes them with one TMA store
+            // of its own, so the write-back is whole-box copies rather than
+            // 16-byte stores that touch a cache line per row, and no warp
+            // waits for another.  Lane 0 waits for its store to have read the
+            // quarter only when the quarter is wanted again.  The O columns
             // are released to the next unit's P.V as soon as the last chunk
-            // has been read out of TMEM.
-            const uint32_t stg = sStg + t * C::kBoxBytes;
-            const uint32_t stg_full = smem_u32(&sh->stg_full[t]);
-            const uint32_t stg_free = smem_u32(&sh->stg_free[t]);
-            const bool issuer = row == 0;
+            // has been read out of tensor memory.
+            const uint32_t stg = sStg + t * C::kBoxBytes + wq * (C::kBoxBytes / 4);
 #pragma unroll 1
-            for (int c = 0; c < D / 64 && ok; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t oa[32], ob[32];
                 tmem_ld32(tO + c * 64, oa);
                 tmem_ld32(tO + c * 64 + 32, ob);
@@ -502,14 +501,10 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                     tc_fence_before();
                     mbar_arrive(o_free);
                 }
-                // The previous store out of this box has read it: its issuer
-                // waits for that only now, when the box is wanted again, so
-                // the wait is off the path that releases O.
-                if (issuer && e_cnt > 0) {
-                    bulk_wait_group_read<0>();
-                    mbar_arrive(stg_free);
+                if (e_cnt > 0) {
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
                 }
-                if (e_cnt > 0 && !(ok = W.wait_warp(stg_free, (e_cnt - 1) & 1))) break;
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) {
                     const uint32_t* w = uu < 4 ? oa + 8 * uu : ob + 8 * (uu - 4);
@@ -517,15 +512,14 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
                                                pack2<kBf16>(u2f(w[2]) * inv, u2f(w[3]) * inv),
                                                pack2<kBf16>(u2f(w[4]) * inv, u2f(w[5]) * inv),
                                                pack2<kBf16>(u2f(w[6]) * inv, u2f(w[7]) * inv));
-                    st_shared_v4(stg + row * 128 + (((uint32_t)uu ^ (uint32_t)(row & 7)) << 4), v);
+                    st_shared_v4(stg + lane * 128 + (((uint32_t)uu ^ (uint32_t)(lane & 7)) << 4), v);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(stg_full);
-                if (issuer && (ok = W.wait(stg_full, e_cnt & 1))) {
-                    tma_store_5d(&p.tm_o, stg, 0, r0, c, un.bh % p.H, un.bh / p.H);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_5d(&p.tm_o, stg, 0, r0 + wq * 32, c, un.bh % p.H, un.bh / p.H);
                     bulk_commit_group();
                 }
-                ok = __all_sync(0xffffffffu, ok);
                 ++e_cnt;
             }
             if (!ok) break;
@@ -533,7 +527,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& p, const Waiter& W,
         if (live && p.lse) p.lse[lrow] = (m_ref + log2f(l)) * kLn2;
     }
     // Every TMA store of O has finished before the CTA's shared memory goes.
-    if (row == 0) bulk_wait_group<0>();
+    if (lane == 0) bulk_wait_group<0>();
 }
 
 template <int D, bool kBf16, bool kPosScale, bool kMask>
@@ -567,8 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_tc_kernel(const __grid_con
             }
             mbar_init(smem_u32(&sh->o_done[t]), 1);
             mbar_init(smem_u32(&sh->o_free[t]), 128);
-            mbar_init(smem_u32(&sh->stg_full[t]), 128);
-            mbar_init(smem_u32(&sh->stg_free[t]), 1);
         }
         mbar_init(smem_u32(&sh->drain[0]), 1);
         mbar_init(smem_u32(&sh->drain[1]), 1);
