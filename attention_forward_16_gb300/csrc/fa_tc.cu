@@ -282,6 +282,23 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
     const uint64_t q_desc = make_sdesc(qa, 16, 1024);
     const uint64_t k_desc = make_sdesc(sKVa, 16, 1024);
     const uint64_t v_desc = make_sdesc(sKVa, C::kBoxBytes, 1024);
+    // A unit's first S has no P.V to interleave with: one N = 128 product
+    // serves both halves, reading Q from shared memory once instead of twice
+    // at the point where the unit's loads and the previous epilogue also use
+    // shared memory.
+    constexpr uint32_t idesc_s2 = make_idesc(kBf16, kTileM, kTileN, false);
+    auto issue_s_full = [&](uint32_t slot) {
+        const uint64_t kb = k_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+            if (leader) mma_ss(dS, q_desc + off, kb + off, idesc_s2, kk > 0);
+        }
+        if (leader) {
+            mma_commit(smem_u32(&sh->s_full[t][0]));
+            mma_commit(smem_u32(&sh->s_full[t][1]));
+        }
+    };
     auto issue_s = [&](uint32_t slot, int h) {
         const uint64_t kb = k_desc + (uint64_t)(slot * (uint32_t)(C::kTileBytes >> 4) + (uint32_t)((h * kHalf * 128) >> 4));
 #pragma unroll
@@ -345,8 +362,7 @@ __device__ __forceinline__ void mma_role(const TcParams& p, const Waiter& W, Sha
         const bool split = kBf16 && kMask && tile_split_p(p.g, un.q0 + t * kTileM);
         for (int j = un.jlo; j < lo && ok; ++j) ok = skip_kv(kidx(j)) && skip_kv(kidx(j) + 1);
         if (!ok || !(ok = wait_kv(kidx(lo)))) break;
-        issue_s(kidx(lo) % C::kStages, 0);
-        issue_s(kidx(lo) % C::kStages, 1);
+        issue_s_full(kidx(lo) % C::kStages);
         if (leader) mma_commit(smem_u32(&sh->kv_empty[kidx(lo) % C::kStages]));
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t v = kidx(j) + 1;
