@@ -244,7 +244,7 @@ __device__ __forceinline__ void zero_row(void* out, size_t row, int pt) {
 }
 
 // ===================================================================== dK, dV
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kMask>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     using M = Mma<D, kBf16>;
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
             tc_fence_after();
             uint32_t s[kChunks][32];
             ld_part(tS, s);
-            const bool masked = tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
+            const bool masked = kMask && tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
             int r_lo = 0, r_hi = kTileM - 1;
             if (masked) key_visible_rows(p.g, kc, i, r_lo, r_hi);
             // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
 }
 
 // ========================================================================= dQ
-template <int D, bool kBf16>
+template <int D, bool kBf16, bool kMask>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = BwdCfg<D>;
     using M = Mma<D, kBf16>;
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dq_kernel(const __grid_
             ld_part(tS, s);
             tc_fence_before();
             mbar_arrive(smem_u32(&sh->s_free[hf]));
-            const bool masked = tile_needs_mask(p.g, r0, j);  // uniform over the CTA
+            const bool masked = kMask && tile_needs_mask(p.g, r0, j);  // uniform over the CTA
             int c_lo = 0, c_hi = kTileN - 1;
             if (masked) row_visible_cols(p.g, qi, j, c_lo, c_hi);
 #pragma unroll
@@ -737,10 +737,13 @@ void launch_pre_typed(const void* o, const void* d_o, const float* lse, float* l
                                                           N, Npad, layout);
 }
 
-template <int D, bool kBf16>
+// kMask = false builds both kernels without the element-mask code, for
+// problems where no tile needs it (geom_needs_masks); as in the forward, the
+// smaller code runs measurably faster.
+template <int D, bool kBf16, bool kMask>
 cudaError_t launch_bwd_typed(const BwdParams& p, int B, cudaStream_t s) {
-    auto kdkdv = fa_bwd_dkdv_kernel<D, kBf16>;
-    auto kdq = fa_bwd_dq_kernel<D, kBf16>;
+    auto kdkdv = fa_bwd_dkdv_kernel<D, kBf16, kMask>;
+    auto kdq = fa_bwd_dq_kernel<D, kBf16, kMask>;
     constexpr int sm1 = dkdv_smem_bytes<D>();
     constexpr int sm2 = dq_smem_bytes<D>();
     cudaError_t e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1);
@@ -772,9 +775,14 @@ cudaError_t launch_bwd_pre(const void* o, const void* d_o, const float* lse, flo
     return cudaGetLastError();
 }
 
+template <int D, bool kBf16>
+cudaError_t launch_bwd_masks(const BwdParams& p, int B, cudaStream_t s) {
+    return geom_needs_masks(p.g) ? launch_bwd_typed<D, kBf16, true>(p, B, s) : launch_bwd_typed<D, kBf16, false>(p, B, s);
+}
+
 cudaError_t launch_bwd(const BwdParams& p, int B, int D, bool bf16, cudaStream_t s) {
-    if (D == 64) return bf16 ? launch_bwd_typed<64, true>(p, B, s) : launch_bwd_typed<64, false>(p, B, s);
-    return bf16 ? launch_bwd_typed<128, true>(p, B, s) : launch_bwd_typed<128, false>(p, B, s);
+    if (D == 64) return bf16 ? launch_bwd_masks<64, true>(p, B, s) : launch_bwd_masks<64, false>(p, B, s);
+    return bf16 ? launch_bwd_masks<128, true>(p, B, s) : launch_bwd_masks<128, false>(p, B, s);
 }
 
 }  // namespace fa
