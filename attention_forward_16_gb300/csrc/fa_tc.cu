@@ -240,8 +240,9 @@ __device__ __forceinline__ void tma_kv_role(const TcParams& p, const Waiter& W, 
 // S_t,h waits for the P.V that reads it, but the other half's S is already
 // computed: the softmax of one half runs while the tensor core works on the
 // other half (of this tile or of the other Q tile), and no step of the softmax
-// waits for its own tile's MMAs.  Issue order per tile:
-//   S(lo,0) S(lo,1) | PV(j,0) S(j+1,0) PV(j,1) S(j+1,1) | ...
+// waits for its own tile's MMAs.  Issue order per tile (S(lo) is one N = 128
+// product that fills both halves):
+//   S(lo) | PV(j,0) S(j+1,0) PV(j,1) S(j+1,1) | ...
 // A K/V ring slot is released once both warps have arrived (count 2); a tile
 // with no work on key tile j still waits for that slot to be full before
 // arriving, which keeps the phases of the ring aligned.  Each Q tile's buffer
