@@ -112,7 +112,7 @@ def _compare(q, k, v, do, mk, wl, wr, dtype, what, layout="bhnd"):
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("N", [128, 200, 384])
+@pytest.mark.parametrize("N", [128, 200, 384, 512])
 def test_backward_matches_oracle(dtype, D, N):
     q, k, v, do = _inputs(1, 2, 2, N, D, dtype, seed=N + D)
     for mk, wl, wr in MASKS:
@@ -163,6 +163,22 @@ def test_backward_rejects():
         bad = list(args)
         bad[idx] = val
         assert fa.fa_bwd(*bad) == code, (idx, val)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+def test_unmasked_build_equals_masked_build(dtype, layout):
+    """With no mask, whole key tiles and N >= 512 the backward kernels run
+    their build without mask code; a window wider than the sequence selects
+    the full build with every key visible.  Same sums in the same order:
+    bit-equal gradients, and the no-mask ones match the oracle."""
+    N, D = 512, 128
+    q, k, v, do = _inputs(1, 4, 2, N, D, dtype, seed=77)
+    plain = _run(q, k, v, do, MASK_NONE, -1, -1, layout)
+    wide = _run(q, k, v, do, MASK_WINDOW, N, N, layout)
+    for a, b in zip(plain, wide):
+        assert torch.equal(a, b)
+    _compare(q, k, v, do, MASK_NONE, -1, -1, dtype, f"unmasked build {dtype} {layout}", layout)
 
 
 FULL = [("f16", MASK_CAUSAL), ("bf16", MASK_NONE)]

@@ -403,7 +403,7 @@ def _to_bhnd(x, layout):
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
 @pytest.mark.parametrize("Hkv", [6, 3, 1])
-@pytest.mark.parametrize("D,N", [(64, 300), (128, 129)])
+@pytest.mark.parametrize("D,N", [(64, 300), (128, 129), (128, 512)])
 def test_layouts_and_grouped_heads(dtype, layout, Hkv, D, N):
     from oracle import attention_grouped
     B, H = 2, 6
@@ -441,6 +441,36 @@ def test_bnhd_benchmark_shape_sampled():
                                      k[b:b + 1, h // 4:h // 4 + 1].double().numpy(),
                                      v[b:b + 1, h // 4:h // 4 + 1].double().numpy(), 1 / math.sqrt(D), MASK_CAUSAL)
         _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ro, rlse, "f16", False, f"bnhd gqa head {(b, h)}")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,N", [(64, 512), (128, 640)])
+@pytest.mark.parametrize("layout", ["bhnd", "bnhd"])
+def test_unmasked_build_equals_masked_build(dtype, D, N, layout):
+    """A problem with no mask, whole key tiles and N >= 512 runs the kernel
+    build without mask and split-P code; a window wider than the sequence
+    selects the full build yet leaves every key visible and every row with
+    N keys.  Both compute the same sums in the same order: bit-equal O and
+    LSE, and both match the oracle."""
+    from oracle import attention_grouped
+    q, k, v = make_qkv(2, 6, N, D, dtype, seed=N + D)
+    k, v = k[:, ::2].contiguous(), v[:, ::2].contiguous()  # grouped heads, 6 -> 3
+    perm = (lambda t: t.permute(0, 2, 1, 3).contiguous()) if layout == "bnhd" else (lambda t: t)
+    outs = []
+    for window in (None, (N, N)):
+        o, lse = fa.attention_fwd(perm(q).cuda(), perm(k).cuda(), perm(v).cuda(), scale=1.0 / math.sqrt(D),
+                                  window=window, layout=layout)
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        outs.append((o.cpu(), lse.cpu()))
+    assert fb.fa_geom_needs_masks(N, MASK_NONE, -1, -1) == 0
+    assert fb.fa_geom_needs_masks(N, MASK_WINDOW, N, N) == 1
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    back = (lambda t: t.permute(0, 2, 1, 3)) if layout == "bnhd" else (lambda t: t)
+    o = back(outs[0][0]).float().numpy().astype(np.float64)
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    ro, rlse = attention_grouped(qd, kd, vd, 1.0 / math.sqrt(D), MASK_NONE, -1, -1)
+    _check(o, outs[0][1].numpy().astype(np.float64), ro, rlse, dtype, False, f"unmasked build {dtype} D={D}")
 
 
 def test_gqa_rejects_bad_head_counts():
