@@ -391,8 +391,7 @@ int fa_decode_gqa(const void* q, const void* k, const void* v, void* o, float* l
     if (lse && !aligned(lse, 4)) return FA_ERR_ALIGN;
     DeviceInfo* dev;
     if ((rc = device_info(&dev)) != FA_OK) return rc;
-    fa::DecodeParams p;
-    std::memset(&p, 0, sizeof(p));
+    fa::DecodeParams p{};
     p.BH = (long long)B * H_kv;
     p.G = G;
     p.Hkv = H_kv;
@@ -447,8 +446,7 @@ int fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, con
     if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4))) return FA_ERR_ALIGN;
     DeviceInfo* dev;
     if ((rc = device_info(&dev)) != FA_OK) return rc;
-    fa::DecodeParams p;
-    std::memset(&p, 0, sizeof(p));
+    fa::DecodeParams p{};
     p.BH = (long long)B * H_kv;
     p.G = G;
     p.Hkv = H_kv;
