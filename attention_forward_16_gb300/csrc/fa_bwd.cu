@@ -34,6 +34,7 @@
 // neither overwrites values the other still reads; the products that read
 // them from TMEM address the halves separately.  Every mbarrier wait is
 // bounded, as in the forward kernel.
+#include <atomic>
 #include <cmath>
 #include <type_traits>
 
@@ -82,6 +83,7 @@ struct __align__(16) BwdCtl {
     // whose parts run on their own barriers; the dK/dV kernel uses index 0.
     uint64_t s_full[kParts], s_free[kParts], dp_full[kParts], p_full[kParts], ds_full[kParts];
     uint64_t acc_done, drain;
+    uint64_t kv_free, acc_free;  // dK/dV: K and V reusable; dV and dK read out of TMEM
     uint32_t tmem_base;
     int abort;
 };
@@ -186,6 +188,8 @@ __device__ __forceinline__ void init_ctl(BwdCtl* sh, int ring_empty_count, int e
     }
     mbar_init(smem_u32(&sh->acc_done), 1);
     mbar_init(smem_u32(&sh->drain), 1);
+    mbar_init(smem_u32(&sh->kv_free), 1);
+    mbar_init(smem_u32(&sh->acc_free), kEwThreads);
     sh->abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -245,8 +249,17 @@ __device__ __forceinline__ void zero_row(void* out, size_t row, int pt) {
 }
 
 // ===================================================================== dK, dV
+// A dK/dV CTA takes `per_cta` consecutive key tiles of the (b, K/V head)-
+// major order, one after the other.  The CTA's set-up is paid once, and the
+// next tile's K/V loads and first S^T / dP^T products run while the
+// elementwise warps write out the previous tile's dK and dV.  Under a mask
+// the tiles' lengths differ and one tile per CTA balances better; without,
+// dkdv_tiles_per_cta picks the count (at most kDkdvMaxTiles).
+constexpr int kDkdvMaxTiles = 4;
+
 template <int D, bool kBf16, bool kMask>
-__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p,
+                                                                      const int n_work, const int per_cta) {
     using C = BwdCfg<D>;
     using M = Mma<D, kBf16>;
     extern __shared__ uint8_t smem_raw[];
@@ -258,15 +271,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);  // warp-uniform to the compiler
     const int lane = threadIdx.x & 31;
 
-    // CTA -> (b, K/V head, key tile j); consecutive CTAs share a head, so the
-    // query tiles they all stream stay in L2
-    const int j = blockIdx.x % p.n_tiles;
-    const int bk = blockIdx.x / p.n_tiles;
-    const int b = bk / p.Hkv, hk = bk % p.Hkv;
-    int ilo, ihi;
-    q_tile_range(p.g, j, ilo, ihi);
-    const int ni = ihi - ilo;
-    const int n_items = ni * p.G;  // (query head of the group, query tile) pairs, head-major
+    // Key tile w -> (b, K/V head, j), its query tiles [ilo, ihi) and its
+    // (query head of the group, query tile) items, head-major.  Every role
+    // derives the same sequence, and tiles without items are skipped by all
+    // but the elementwise warps (which write their zero gradients).
+    struct Tile {
+        int j, b, hk, ilo, ni, n_items;
+    };
+    auto tile = [&](int t) {
+        Tile tl;
+        const int w = per_cta * (int)blockIdx.x + t;
+        tl.j = w % p.n_tiles;
+        const int bk = w / p.n_tiles;
+        tl.b = bk / p.Hkv;
+        tl.hk = bk % p.Hkv;
+        int ihi;
+        q_tile_range(p.g, tl.j, tl.ilo, ihi);
+        tl.ni = ihi - tl.ilo;
+        tl.n_items = tl.ni * p.G;
+        return tl;
+    };
+    // (the masked build always takes one tile: a compile-time count lets the
+    // compiler drop the cross-tile waits)
+    const int n_mine = kMask ? 1
+                             : (n_work - per_cta * (int)blockIdx.x < per_cta ? n_work - per_cta * (int)blockIdx.x
+                                                                             : per_cta);
 
     if (threadIdx.x == 0) init_ctl(sh, 1, kEwThreads);
     if (warp == kWarpMmaB) {
@@ -278,77 +307,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, sh->tmem_base, 0);
     const Waiter W{&sh->abort, p.status, p.wait_limit_ns};
-    auto item = [&](int n, int& h, int& i) {
-        h = hk * p.G + n / ni;
-        i = ilo + n % ni;
-    };
 
-    if (warp == kWarpTmaB && lane == 0 && n_items > 0) {
+    if (warp == kWarpTmaB && lane == 0) {
         // ------------------------------------------------------------ TMA
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_do);
         const uint32_t fixed = smem_u32(&sh->fixed_full);
-        mbar_arrive_expect_tx(fixed, 2 * C::kTileBytes);
-        load_tile<D>(sK, &p.tm_k, fixed, p.layout, b, hk, j * kTileN);
-        load_tile<D>(sV, &p.tm_v, fixed, p.layout, b, hk, j * kTileN);
         bool ok = true;
-        int n = 0;
-        for (; n < n_items && ok; ++n) {
-            const int st = n % C::kStages;
-            if (n >= C::kStages && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((n / C::kStages) - 1) & 1))) break;
-            int h, i;
-            item(n, h, i);
-            const uint32_t full = smem_u32(&sh->ring_full[st]);
-            const uint32_t stage = sRing + st * C::kStageKV;
-            mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 2 * C::kVecBytes);
-            load_tile<D>(stage, &p.tm_q, full, p.layout, b, h, i * kTileM);
-            load_tile<D>(stage + C::kTileBytes, &p.tm_do, full, p.layout, b, h, i * kTileM);
-            const size_t vrow = ((size_t)b * p.H + h) * p.Npad + (size_t)i * kTileM;
-            bulk_load(stage + 2 * C::kTileBytes, p.lse2 + vrow, C::kVecBytes, full);
-            bulk_load(stage + 2 * C::kTileBytes + C::kVecBytes, p.dsum + vrow, C::kVecBytes, full);
+        int g = 0;   // ring position across tiles
+        int ti = 0;  // tiles with items so far
+        for (int t = 0; t < n_mine && ok; ++t) {
+            const Tile tl = tile(t);
+            if (tl.n_items == 0) continue;
+            // K and V of the previous tile are free once its last S^T and dP^T
+            // have completed.
+            if (ti > 0 && !(ok = W.wait(smem_u32(&sh->kv_free), (ti - 1) & 1))) break;
+            mbar_arrive_expect_tx(fixed, 2 * C::kTileBytes);
+            load_tile<D>(sK, &p.tm_k, fixed, p.layout, tl.b, tl.hk, tl.j * kTileN);
+            load_tile<D>(sV, &p.tm_v, fixed, p.layout, tl.b, tl.hk, tl.j * kTileN);
+            ++ti;
+            for (int n = 0; n < tl.n_items && ok; ++n, ++g) {
+                const int st = g % C::kStages;
+                if (g >= C::kStages && !(ok = W.wait(smem_u32(&sh->ring_empty[st]), ((g / C::kStages) - 1) & 1)))
+                    break;
+                const int h = tl.hk * p.G + n / tl.ni, i = tl.ilo + n % tl.ni;
+                const uint32_t full = smem_u32(&sh->ring_full[st]);
+                const uint32_t stage = sRing + st * C::kStageKV;
+                mbar_arrive_expect_tx(full, 2 * C::kTileBytes + 2 * C::kVecBytes);
+                load_tile<D>(stage, &p.tm_q, full, p.layout, tl.b, h, i * kTileM);
+                load_tile<D>(stage + C::kTileBytes, &p.tm_do, full, p.layout, tl.b, h, i * kTileM);
+                const size_t vrow = ((size_t)tl.b * p.H + h) * p.Npad + (size_t)i * kTileM;
+                bulk_load(stage + 2 * C::kTileBytes, p.lse2 + vrow, C::kVecBytes, full);
+                bulk_load(stage + 2 * C::kTileBytes + C::kVecBytes, p.dsum + vrow, C::kVecBytes, full);
+            }
         }
         // let every issued copy land before the CTA releases shared memory
-        W.drain(fixed, 0);
-        for (int m = n - C::kStages < 0 ? 0 : n - C::kStages; m < n; ++m)
+        if (ti > 0) W.drain(fixed, (ti - 1) & 1);
+        for (int m = g - C::kStages < 0 ? 0 : g - C::kStages; m < g; ++m)
             W.drain(smem_u32(&sh->ring_full[m % C::kStages]), (m / C::kStages) & 1);
-    } else if (warp == kWarpMmaB && n_items > 0) {
+    } else if (warp == kWarpMmaB) {
         // ------------------------------------------------------------ MMA
         // The whole warp follows one path; the elected lane issues.
         const bool leader = elect_one();
         const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
         const uint32_t tDV = tmem + C::kColA, tDK = tmem + C::kColB;
-        auto stage = [&](int n) { return sRing + (n % C::kStages) * C::kStageKV; };
-        auto ring_full = [&](int n) {
-            return W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1);
+        auto stage = [&](int g) { return sRing + (g % C::kStages) * C::kStageKV; };
+        auto ring_full = [&](int g) {
+            return W.wait_warp(smem_u32(&sh->ring_full[g % C::kStages]), (g / C::kStages) & 1);
         };
-        bool ok = W.wait_warp(smem_u32(&sh->fixed_full), 0) && ring_full(0);
-        if (ok) {
+        bool ok = true;
+        int g = 0;   // ring position (and item count) across tiles
+        int ti = 0;
+        for (int t = 0; t < n_mine && ok; ++t) {
+            const Tile tl = tile(t);
+            if (tl.n_items == 0) continue;
+            if (!(ok = W.wait_warp(smem_u32(&sh->fixed_full), ti & 1) && ring_full(g))) break;
             tc_fence_after();
-            M::rows(tS, sK, stage(0), leader);                       // S^T = K Q^T
+            M::rows(tS, sK, stage(g), leader);                       // S^T = K Q^T
             if (leader) mma_commit(smem_u32(&sh->s_full[0]));
-            M::rows(tDP, sV, stage(0) + C::kTileBytes, leader);      // dP^T = V dO^T
+            M::rows(tDP, sV, stage(g) + C::kTileBytes, leader);      // dP^T = V dO^T
             if (leader) mma_commit(smem_u32(&sh->dp_full[0]));
-        }
-        for (int n = 0; n < n_items && ok; ++n) {
-            if (!(ok = W.wait_warp(smem_u32(&sh->p_full[0]), n & 1))) break;
-            tc_fence_after();
-            M::cols(tDV, tS, stage(n) + C::kTileBytes, n > 0, leader);   // dV += P^T dO
-            if (n + 1 < n_items) {
-                if (!(ok = ring_full(n + 1))) break;
+            for (int n = 0; n < tl.n_items && ok; ++n, ++g) {
+                if (!(ok = W.wait_warp(smem_u32(&sh->p_full[0]), g & 1))) break;
+                // dV and dK of the previous tile have been read out of TMEM
+                if (n == 0 && ti > 0 && !(ok = W.wait_warp(smem_u32(&sh->acc_free), (ti - 1) & 1))) break;
                 tc_fence_after();
-                M::rows(tS, sK, stage(n + 1), leader);
-                if (leader) mma_commit(smem_u32(&sh->s_full[0]));
+                M::cols(tDV, tS, stage(g) + C::kTileBytes, n > 0, leader);   // dV += P^T dO
+                if (n + 1 < tl.n_items) {
+                    if (!(ok = ring_full(g + 1))) break;
+                    tc_fence_after();
+                    M::rows(tS, sK, stage(g + 1), leader);
+                    if (leader) mma_commit(smem_u32(&sh->s_full[0]));
+                }
+                if (!(ok = W.wait_warp(smem_u32(&sh->ds_full[0]), g & 1))) break;
+                tc_fence_after();
+                M::cols(tDK, tDP, stage(g), n > 0, leader);                  // dK += dS^T Q
+                if (leader) mma_commit(smem_u32(&sh->ring_empty[g % C::kStages]));
+                if (n + 1 < tl.n_items) {
+                    M::rows(tDP, sV, stage(g + 1) + C::kTileBytes, leader);
+                    if (leader) mma_commit(smem_u32(&sh->dp_full[0]));
+                }
             }
-            if (!(ok = W.wait_warp(smem_u32(&sh->ds_full[0]), n & 1))) break;
-            tc_fence_after();
-            M::cols(tDK, tDP, stage(n), n > 0, leader);                  // dK += dS^T Q
-            if (leader) mma_commit(smem_u32(&sh->ring_empty[n % C::kStages]));
-            if (n + 1 < n_items) {
-                M::rows(tDP, sV, stage(n + 1) + C::kTileBytes, leader);
-                if (leader) mma_commit(smem_u32(&sh->dp_full[0]));
-            }
+            if (!ok) break;
+            // every product of the tile is issued: K and V go back to the
+            // loader, dV and dK to the epilogue, once they complete
+            if (leader) mma_commit(smem_u32(&sh->kv_free));
+            if (leader) mma_commit(smem_u32(&sh->acc_done));
+            ++ti;
         }
-        if (leader) mma_commit(smem_u32(&sh->acc_done));
         if (leader) mma_commit(smem_u32(&sh->drain));
         W.drain(smem_u32(&sh->drain), 0);
     } else if (warp >= kWarpEw0) {
@@ -356,104 +402,114 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_dkdv_kernel(const __gri
         const int wq = (warp - kWarpEw0) & 3;   // TMEM lane quarter
         const int hf = (warp - kWarpEw0) >> 2;  // query-column part of the tile
         const int c = wq * 32 + lane;           // key row within the tile
-        const int kc = j * kTileN + c;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + C::kColS + hf * kColsPerPart;
         const uint32_t tDP = tmem + lane_base + C::kColDP + hf * kColsPerPart;
         const float c2 = p.scale_log2;
         bool ok = true;
-        for (int n = 0; n < n_items && ok; ++n) {
-            int h, i;
-            item(n, h, i);
-            const uint8_t* stage = smem + 2 * C::kTileBytes + (n % C::kStages) * C::kStageKV;
-            const float4* lse2 = reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes) + hf * (kColsPerPart / 4);
-            const float4* dsum =
-                reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * (kColsPerPart / 4);
-            if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[n % C::kStages]), (n / C::kStages) & 1))) break;
-            if (!(ok = W.wait_warp(smem_u32(&sh->s_full[0]), n & 1))) break;
-            tc_fence_after();
-            uint32_t s[kChunks][32];
-            ld_part(tS, s);
-            const bool masked = kMask && tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
-            int r_lo = 0, r_hi = kTileM - 1;
-            if (masked) key_visible_rows(p.g, kc, i, r_lo, r_hi);
-            // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
-            auto pt = [&](auto kM) {
-                constexpr bool M = decltype(kM)::value;
+        int g = 0;
+        int ti = 0;
+        for (int t = 0; t < n_mine && ok; ++t) {
+            const Tile tl = tile(t);
+            const int j = tl.j;
+            const int kc = j * kTileN + c;
+            for (int n = 0; n < tl.n_items && ok; ++n, ++g) {
+                const int i = tl.ilo + n % tl.ni;
+                const uint8_t* stage = smem + 2 * C::kTileBytes + (g % C::kStages) * C::kStageKV;
+                const float4* lse2 =
+                    reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes) + hf * (kColsPerPart / 4);
+                const float4* dsum =
+                    reinterpret_cast<const float4*>(stage + 2 * C::kTileBytes + C::kVecBytes) + hf * (kColsPerPart / 4);
+                if (!(ok = W.wait_warp(smem_u32(&sh->ring_full[g % C::kStages]), (g / C::kStages) & 1))) break;
+                if (!(ok = W.wait_warp(smem_u32(&sh->s_full[0]), g & 1))) break;
+                tc_fence_after();
+                uint32_t s[kChunks][32];
+                ld_part(tS, s);
+                const bool masked = kMask && tile_needs_mask(p.g, i * kTileM, j);  // uniform over the CTA
+                int r_lo = 0, r_hi = kTileM - 1;
+                if (masked) key_visible_rows(p.g, kc, i, r_lo, r_hi);
+                // P^T: p = 2^(s * scale * log2 e - LSE_q * log2 e), 0 where masked
+                auto pt = [&](auto kM) {
+                    constexpr bool M = decltype(kM)::value;
+#pragma unroll
+                    for (int cc = 0; cc < kChunks; ++cc) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float4 l4 = lds_f4(lse2 + cc * 8 + v);
+                            float e0, e1, e2, e3;
+                            ffma2(e0, e1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]), c2, c2, -l4.x, -l4.y);
+                            ffma2(e2, e3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]), c2, c2, -l4.z, -l4.w);
+                            e0 = ex2(e0);
+                            e1 = ex2(e1);
+                            e2 = ex2(e2);
+                            e3 = ex2(e3);
+                            if (M) {
+                                const int q = hf * kColsPerPart + cc * 32 + 4 * v;
+                                if (q < r_lo || q > r_hi) e0 = 0.f;
+                                if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
+                                if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
+                                if (q + 3 < r_lo || q + 3 > r_hi) e3 = 0.f;
+                            }
+                            s[cc][4 * v] = f2u(e0);
+                            s[cc][4 * v + 1] = f2u(e1);
+                            s[cc][4 * v + 2] = f2u(e2);
+                            s[cc][4 * v + 3] = f2u(e3);
+                            pk[2 * v] = pack2<kBf16>(e0, e1);
+                            pk[2 * v + 1] = pack2<kBf16>(e2, e3);
+                        }
+                        tmem_st16(tS + 16 * cc, pk);
+                    }
+                };
+                // Two copies of the loop, one without the per-element test: a tile
+                // needs the mask only on the diagonal or a band's edge, and the test
+                // kept in the common copy cost the causal backward 12%.
+                if (masked) pt(std::true_type{}); else pt(std::false_type{});
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sh->p_full[0]));
+                // dS^T: p * (dP - Dsum_q), written over dP columns of this half already read
+                if (!(ok = W.wait_warp(smem_u32(&sh->dp_full[0]), g & 1))) break;
+                tc_fence_after();
+                uint32_t d[kChunks][32];
+                ld_part(tDP, d);
 #pragma unroll
                 for (int cc = 0; cc < kChunks; ++cc) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
-                        const float4 l4 = lds_f4(lse2 + cc * 8 + v);
-                        float e0, e1, e2, e3;
-                        ffma2(e0, e1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]), c2, c2, -l4.x, -l4.y);
-                        ffma2(e2, e3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]), c2, c2, -l4.z, -l4.w);
-                        e0 = ex2(e0);
-                        e1 = ex2(e1);
-                        e2 = ex2(e2);
-                        e3 = ex2(e3);
-                        if (M) {
-                            const int q = hf * kColsPerPart + cc * 32 + 4 * v;
-                            if (q < r_lo || q > r_hi) e0 = 0.f;
-                            if (q + 1 < r_lo || q + 1 > r_hi) e1 = 0.f;
-                            if (q + 2 < r_lo || q + 2 > r_hi) e2 = 0.f;
-                            if (q + 3 < r_lo || q + 3 > r_hi) e3 = 0.f;
-                        }
-                        s[cc][4 * v] = f2u(e0);
-                        s[cc][4 * v + 1] = f2u(e1);
-                        s[cc][4 * v + 2] = f2u(e2);
-                        s[cc][4 * v + 3] = f2u(e3);
-                        pk[2 * v] = pack2<kBf16>(e0, e1);
-                        pk[2 * v + 1] = pack2<kBf16>(e2, e3);
+                        const float4 d4 = lds_f4(dsum + cc * 8 + v);
+                        float g0, g1, g2, g3;
+                        fadd2(g0, g1, u2f(d[cc][4 * v]), u2f(d[cc][4 * v + 1]), -d4.x, -d4.y);
+                        fadd2(g2, g3, u2f(d[cc][4 * v + 2]), u2f(d[cc][4 * v + 3]), -d4.z, -d4.w);
+                        fmul2(g0, g1, g0, g1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]));
+                        fmul2(g2, g3, g2, g3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]));
+                        pk[2 * v] = pack2<kBf16>(g0, g1);
+                        pk[2 * v + 1] = pack2<kBf16>(g2, g3);
                     }
-                    tmem_st16(tS + 16 * cc, pk);
+                    tmem_st16(tDP + 16 * cc, pk);
                 }
-            };
-            // Two copies of the loop, one without the per-element test: a tile
-            // needs the mask only on the diagonal or a band's edge, and the test
-            // kept in the common copy cost the causal backward 12%.
-            if (masked) pt(std::true_type{}); else pt(std::false_type{});
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sh->p_full[0]));
-            // dS^T: p * (dP - Dsum_q), written over dP columns of this half already read
-            if (!(ok = W.wait_warp(smem_u32(&sh->dp_full[0]), n & 1))) break;
-            tc_fence_after();
-            uint32_t d[kChunks][32];
-            ld_part(tDP, d);
-#pragma unroll
-            for (int cc = 0; cc < kChunks; ++cc) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const float4 d4 = lds_f4(dsum + cc * 8 + v);
-                    float g0, g1, g2, g3;
-                    fadd2(g0, g1, u2f(d[cc][4 * v]), u2f(d[cc][4 * v + 1]), -d4.x, -d4.y);
-                    fadd2(g2, g3, u2f(d[cc][4 * v + 2]), u2f(d[cc][4 * v + 3]), -d4.z, -d4.w);
-                    fmul2(g0, g1, g0, g1, u2f(s[cc][4 * v]), u2f(s[cc][4 * v + 1]));
-                    fmul2(g2, g3, g2, g3, u2f(s[cc][4 * v + 2]), u2f(s[cc][4 * v + 3]));
-                    pk[2 * v] = pack2<kBf16>(g0, g1);
-                    pk[2 * v + 1] = pack2<kBf16>(g2, g3);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sh->ds_full[0]));
+            }
+            // epilogue: this part's columns of dV and scale * dK for the keys that exist
+            const bool live = kc < p.g.N;
+            const size_t row = (size_t)row_index(p.layout, tl.b, tl.hk, live ? kc : 0, p.Hkv, p.g.N);
+            if (tl.n_items == 0) {
+                if (live) {
+                    zero_row<D>(p.dv, row, hf);
+                    zero_row<D>(p.dk, row, hf);
                 }
-                tmem_st16(tDP + 16 * cc, pk);
+            } else if (ok && (ok = W.wait_warp(smem_u32(&sh->acc_done), ti & 1))) {
+                tc_fence_after();
+                store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dv, row, hf, 1.f, live);
+                store_row<D, kBf16>(tmem + lane_base + C::kColB, p.dk, row, hf, p.scale, live);
+                // the accumulators may now take the next tile's products
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sh->acc_free));
+                ++ti;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sh->ds_full[0]));
-        }
-        // epilogue: this part's columns of dV and scale * dK for the keys that exist
-        const bool live = kc < p.g.N;
-        const size_t row = (size_t)row_index(p.layout, b, hk, live ? kc : 0, p.Hkv, p.g.N);
-        if (n_items == 0) {
-            if (live) {
-                zero_row<D>(p.dv, row, hf);
-                zero_row<D>(p.dk, row, hf);
-            }
-        } else if (ok && W.wait_warp(smem_u32(&sh->acc_done), 0)) {
-            tc_fence_after();
-            store_row<D, kBf16>(tmem + lane_base + C::kColA, p.dv, row, hf, 1.f, live);
-            store_row<D, kBf16>(tmem + lane_base + C::kColB, p.dk, row, hf, p.scale, live);
         }
     }
 
@@ -749,6 +805,37 @@ void launch_pre_typed(const void* o, const void* d_o, const float* lse, float* l
                                                           N, Npad, layout);
 }
 
+// Key tiles per dK/dV CTA for a problem without masks (each key tile then has
+// `items` query tiles): the count k that minimises (waves of CTAs) x (k + a),
+// one CTA per SM, where a = 4.8 / items is a CTA's fixed cost (set-up and
+// last epilogue) in units of one key tile's work, measured at about 0.15 for
+// 32 query tiles.  At B = 4, H = 32, N = 4096 on 152 SMs this picks 3 (4,096
+// key tiles in 1,366 CTAs, 8.98 waves); measured, 1 to 4 tiles per CTA took
+// 2.66, 2.60, 2.54 and 2.58 ms a backward call.
+int dkdv_tiles_per_cta(long long n_work, int items) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> sm_count[kMaxDev];
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 1;
+    sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms <= 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 1;
+        sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
+    const double a = 4.8 / (items > 0 ? items : 1);
+    int best = 1;
+    double best_cost = 0.0;
+    for (int k = 1; k <= kDkdvMaxTiles; ++k) {
+        const long long ctas = (n_work + k - 1) / k;
+        const double cost = (double)((ctas + sms - 1) / sms) * (k + a);
+        if (k == 1 || cost < best_cost) {
+            best = k;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 // kMask = false builds both kernels without the element-mask code, for
 // problems where no tile needs it (geom_needs_masks); as in the forward, the
 // smaller code runs measurably faster.
@@ -762,7 +849,10 @@ cudaError_t launch_bwd_typed(const BwdParams& p, int B, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2);
     if (e != cudaSuccess) return e;
-    kdkdv<<<B * p.Hkv * p.n_tiles, kBwdThreads, sm1, s>>>(p);
+    const long long n_work = (long long)B * p.Hkv * p.n_tiles;  // key tiles
+    const int per_cta = kMask ? 1 : dkdv_tiles_per_cta(n_work, p.n_tiles * p.G);
+    if (n_work > 0x7fffffffLL - per_cta) return cudaErrorInvalidValue;
+    kdkdv<<<(unsigned)((n_work + per_cta - 1) / per_cta), kBwdThreads, sm1, s>>>(p, (int)n_work, per_cta);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kdq<<<B * p.H * p.n_tiles, kBwdThreads, sm2, s>>>(p);
     return cudaGetLastError();
